@@ -1,0 +1,74 @@
+// moe_internal.h -- host-side declarations shared by the library's
+// translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Bits ORed into the workspace status word by kernels.
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBounds = 2u;
+
+constexpr int kRowBlock = 128;      // rows per expert block (the expert alignment unit)
+constexpr int kChunkTokens = 32;    // tokens per routing histogram chunk (one warp)
+
+inline int64_t max_blocks_of(const moe_shape& s) {
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  const int64_t touched = R < s.E ? R : s.E;
+  return (R + (kRowBlock - 1) * touched) / kRowBlock;
+}
+inline int64_t max_rows_of(const moe_shape& s) { return kRowBlock * max_blocks_of(s); }
+inline int64_t num_chunks_of(const moe_shape& s) { return (s.T + kChunkTokens - 1) / kChunkTokens; }
+
+// Byte offsets of everything the workspace holds.
+struct WsLayout {
+  size_t status;        // uint32 status word (+ padding)
+  size_t chunk_counts;  // int32 [E][num_chunks]: per-chunk expert histogram, later chunk bases
+  size_t xp;            // bf16 [max_rows][H]: gathered activation rows
+  size_t topk_ids, topk_w, counts, off_pad, block_expert, num_blocks, gather_idx, scatter_idx;
+  size_t h;             // bf16 [max_rows][I]
+  size_t y;             // bf16 [max_rows][H]
+  size_t total;
+};
+WsLayout ws_layout(const moe_shape& s);
+
+inline uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
+
+// Launchers (asynchronous; return cudaGetLastError()).
+cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
+                         int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
+                         int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
+                         uint32_t* status, cudaStream_t st);
+
+cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx,
+                                const int32_t* num_blocks, uint16_t* Xp, uint32_t* status, cudaStream_t st);
+
+struct GemmMaps {
+  CUtensorMap a;     // A operand rows (K-major): Xp [max_rows][H] or h [max_rows][I]
+  CUtensorMap b0;    // up: W_gate [E*H][I]; down: W_down [E*I][H]
+  CUtensorMap b1;    // up: W_up   [E*H][I]; down: unused (copy of b0)
+  CUtensorMap d;     // output rows: h [max_rows][I] or Y [max_rows][H]
+};
+
+cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
+                           const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status,
+                           int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
+                             const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status,
+                             int num_sms, cudaStream_t st);
+
+cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
+                           const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda).
+// rows x cols bf16 row-major, box = box_cols (inner) x box_rows, 128-byte swizzle.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols);
+
+}  // namespace moe
