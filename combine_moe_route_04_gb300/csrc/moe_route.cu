@@ -43,6 +43,18 @@ struct Cand {
   float x;   // exp(logit - max)
 };
 
+// exp(v - m) for float32 v <= m: the difference is split exactly into
+// d_hi + d_lo (2Sum) and exp(d_hi + d_lo) ~= exp(d_hi) * (1 + d_lo), so the
+// result carries expf's error only, not the rounding of v - m (which grows
+// with |v - m|).
+__device__ __forceinline__ float exp_diff(float v, float m) {
+  const float d_hi = v - m;
+  const float bb = d_hi - v;
+  const float d_lo = (v - (d_hi - bb)) + (-m - bb);
+  const float e = expf(d_hi);
+  return fmaf(e, d_lo, e);
+}
+
 __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
   return va > vb || (va == vb && ea < eb);
 }
@@ -78,7 +90,7 @@ __global__ void __launch_bounds__(1024) route_topk_hist_kernel(const float* __re
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 #pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) x[i] = (lane + 32 * i < E) ? expf(v[i] - m) : 0.0f;
+    for (int i = 0; i < kMaxEPerLane; ++i) x[i] = (lane + 32 * i < E) ? exp_diff(v[i], m) : 0.0f;
 
     uint32_t taken = 0;  // bit i: element i of this lane already picked
     int my_id = 0;
@@ -106,9 +118,16 @@ __global__ void __launch_bounds__(1024) route_topk_hist_kernel(const float* __re
       }
     }
     // renormalise over the picks: w_j = x_j / sum_{j' in slot order} x_j'
-    // (the softmax denominator cancels)
-    float S = 0.0f;
-    for (int j = 0; j < k; ++j) S += __shfl_sync(0xffffffffu, my_x, j);
+    // (the softmax denominator cancels).  Slots hold non-increasing x, so
+    // Fast2Sum keeps the rounding error of each addition.
+    float S = 0.0f, comp = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const float y = __shfl_sync(0xffffffffu, my_x, j);
+      const float t = S + y;
+      comp += (S - t) + y;
+      S = t;
+    }
+    S += comp;
     if (lane < k) {
       topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
       topk_w[static_cast<int64_t>(t) * k + lane] = my_x / S;
