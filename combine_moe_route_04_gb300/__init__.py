@@ -22,12 +22,12 @@ _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
-                6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS"}
+                6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS", 8: "MOE_ERR_SCRATCH_LIMIT"}
 
 # every function include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_init",
            "moe_last_device_status", "moe_route", "moe_grouped_gemm_up", "moe_grouped_gemm_down",
-           "moe_combine", "moe_forward", "moe_workspace_views"]
+           "moe_combine", "moe_forward", "moe_workspace_views", "moe_route_noalloc"]
 
 
 class MoEError(RuntimeError):
@@ -79,6 +79,8 @@ def load():
     lib.moe_last_device_status.argtypes = [P, P]
     lib.moe_route.restype = st
     lib.moe_route.argtypes = [S] + [P] * 11
+    lib.moe_route_noalloc.restype = st
+    lib.moe_route_noalloc.argtypes = [S] + [P] * 10
     lib.moe_grouped_gemm_up.restype = st
     lib.moe_grouped_gemm_up.argtypes = [S] + [P] * 10
     lib.moe_grouped_gemm_down.restype = st
@@ -212,6 +214,25 @@ def moe_route(s, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_bl
             _dev_tensor(scatter_idx, torch.int32, s.T * s.k, "scatter_idx"),
             _dev_tensor(ws, torch.uint8, workspace_size(s), "ws")]
     _check(load().moe_route(ctypes.byref(s), *args, _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(s, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
+                      gather_idx, scatter_idx, stream=None):
+    """moe_route without a workspace (fixed library-owned scratch; see
+    include/moe.h for its size limit and the rule that overlapping calls race)."""
+    import torch
+    s = _shape_obj(s)
+    mb, mr = capacity(s)
+    args = [_dev_tensor(logits, torch.float32, s.T * s.E, "logits"),
+            _dev_tensor(topk_ids, torch.int32, s.T * s.k, "topk_ids"),
+            _dev_tensor(topk_w, torch.float32, s.T * s.k, "topk_w"),
+            _dev_tensor(counts, torch.int32, s.E, "counts"),
+            _dev_tensor(off_pad, torch.int32, s.E + 1, "off_pad"),
+            _dev_tensor(block_expert, torch.int32, mb, "block_expert"),
+            _dev_tensor(num_blocks, torch.int32, 1, "num_blocks"),
+            _dev_tensor(gather_idx, torch.int32, mr, "gather_idx"),
+            _dev_tensor(scatter_idx, torch.int32, s.T * s.k, "scatter_idx")]
+    _check(load().moe_route_noalloc(ctypes.byref(s), *args, _stream(stream)), "moe_route_noalloc")
 
 
 def moe_grouped_gemm_up(s, X, gather_idx, off_pad, block_expert, num_blocks, W_gate, W_up, h, ws,

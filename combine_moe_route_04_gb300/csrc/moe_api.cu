@@ -136,6 +136,9 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* off_pa
 
 }  // namespace
 
+moe_status device_ready(cudaStream_t st, int* num_sms) { return prepare_device(st, num_sms); }
+moe_status validate_shape(const moe_shape* s) { return check_shape(s); }
+
 WsLayout ws_layout(const moe_shape& s) {
   WsLayout L{};
   const size_t T = static_cast<size_t>(s.T), E = static_cast<size_t>(s.E), k = static_cast<size_t>(s.k);
@@ -194,6 +197,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+    case MOE_ERR_SCRATCH_LIMIT: return "MOE_ERR_SCRATCH_LIMIT";
   }
   return "MOE_ERR_UNKNOWN";
 }

@@ -38,6 +38,12 @@ struct WsLayout {
 };
 WsLayout ws_layout(const moe_shape& s);
 
+// Makes the stream's device current and checks it (compute capability 10.3);
+// fetches the tensor-map encoder on first use.
+moe_status device_ready(cudaStream_t st, int* num_sms);
+// The shape checks every entry point applies (MOE_OK or the error code).
+moe_status validate_shape(const moe_shape* s);
+
 inline uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 // Launchers (asynchronous; return cudaGetLastError()).

@@ -26,6 +26,7 @@
 // logits.
 #include <cfloat>
 #include <cstdint>
+#include <mutex>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -293,3 +294,66 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_route_noalloc: moe_route for callers that may not allocate device
+// memory (for instance a plugin whose host framework owns all device memory
+// and only hands it input and output buffers, or a deployment that reserves
+// its memory up front and forbids allocation once running).  The only scratch
+// the routing kernels need -- the per-chunk expert histograms, later the
+// chunk bases -- lives in this fixed array instead of a caller workspace.  It
+// is placed in device memory when the library's module is loaded on a device
+// and stays there until the process exits.
+namespace moe {
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = int64_t(1) << 18;  // 1 MiB of int32
+
+__device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
+
+int32_t* g_route_scratch_addr[64] = {};
+std::mutex g_route_scratch_mu;
+
+// Device address of g_route_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+int32_t* route_scratch_on_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+  if (g_route_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_route_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_route_scratch_addr[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const moe_shape* shape, const float* logits, int32_t* topk_ids,
+                                        float* topk_w, int32_t* counts, int32_t* off_pad, int32_t* block_expert,
+                                        int32_t* num_blocks, int32_t* gather_idx, int32_t* scatter_idx,
+                                        moe_stream_t stream) {
+  using namespace moe;
+  moe_status st = validate_shape(shape);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks, gather_idx,
+                        scatter_idx};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_MISALIGNED;
+  }
+  if (static_cast<int64_t>(shape->E) * num_chunks_of(*shape) > kNoAllocScratchInts) return MOE_ERR_SCRATCH_LIMIT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = device_ready(s, nullptr);  // makes the stream's device current
+  if (st != MOE_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  int32_t* scratch = route_scratch_on_device(dev);
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  // Every chunk-histogram entry the scan and scatter read is written by the
+  // first kernel of this call, so stale contents need no clearing.
+  const cudaError_t e = launch_route(*shape, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
+                                     gather_idx, scatter_idx, scratch, /*status=*/nullptr, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

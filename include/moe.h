@@ -64,7 +64,8 @@ typedef enum {
     MOE_ERR_ARCH = 4,               /* device is not compute capability 10.3 */
     MOE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
     MOE_ERR_TIMEOUT = 6,            /* a kernel's bounded wait ran out */
-    MOE_ERR_DEVICE_BOUNDS = 7       /* a kernel met an index out of range */
+    MOE_ERR_DEVICE_BOUNDS = 7,      /* a kernel met an index out of range */
+    MOE_ERR_SCRATCH_LIMIT = 8       /* moe_route_noalloc: shape needs more than its fixed scratch */
 } moe_status;
 
 typedef struct {
@@ -113,6 +114,34 @@ moe_status moe_route(const moe_shape *shape, const float *logits,
                      int32_t *off_pad, int32_t *block_expert, int32_t *num_blocks,
                      int32_t *gather_idx, int32_t *scatter_idx, void *ws,
                      moe_stream_t stream);
+
+/* moe_route without a workspace: the same kernels and the same outputs as
+ * moe_route, but the per-chunk expert histograms live in a fixed scratch
+ * array that the library places in device memory when it is loaded, so the
+ * caller passes only the inputs and outputs and nothing is allocated.  For
+ * callers that are not allowed to allocate device memory: a plugin whose host
+ * framework owns all device memory and hands it only its inputs and outputs,
+ * or a deployment that reserves its memory up front and forbids allocation
+ * once running (cudaMalloc may also synchronise the device and stall other
+ * streams).  The pages describe no such variant; it has no counterpart there.
+ *   - Limit: E * ceil(T/32) <= 262144 (1 MiB of int32 scratch; e.g. E=128
+ *     with T up to 65536, E=256 with T up to 32768); larger shapes return
+ *     MOE_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - The scratch is one array per device, shared by every call and held
+ *     until the process exits.  Calls whose work may overlap on the GPU (on
+ *     different streams without ordering) race on it; order them on one
+ *     stream.  Every scratch entry a call reads is written earlier in the
+ *     same call, so nothing needs clearing between calls.
+ *   - The first call on a device looks up the scratch address on that device
+ *     (a host-side query, no allocation); make that first call before any
+ *     stream capture.
+ *   - Kernel-side errors are not reported (there is no status word).
+ * Arguments as moe_route, without ws. */
+moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
+                             int32_t *topk_ids, float *topk_w, int32_t *counts,
+                             int32_t *off_pad, int32_t *block_expert, int32_t *num_blocks,
+                             int32_t *gather_idx, int32_t *scatter_idx,
+                             moe_stream_t stream);
 
 /* Step 3: grouped gate/up GEMM with the SiLU(gate)*up epilogue.
  *   X      [T, H] bf16 tokens; rows are gathered through gather_idx
