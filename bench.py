@@ -376,14 +376,52 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_profile(args, local):
+    """Warm-up forwards plus one forward of the chosen workload (for ncu)."""
+    import numpy as np
+    import torch
+
+    import combine_moe_route_04_gb300 as moe
+    import moe_inputs
+    from combine_moe_route_04_gb300 import _build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    cfg = moe_inputs.config(args.workload)
+    inp = moe_inputs.make_inputs(cfg)
+    s = moe.shape(*cfg.shape)
+
+    def up_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x, wg, wu, wd = (up_bf16(inp[n]) for n in ("x", "w_gate", "w_up", "w_down"))
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    ws = moe.alloc_workspace(s, dev)
+    for _ in range(args.warmup + 1):
+        moe.moe_forward(s, logits, x, wg, wu, wd, out, ws)
+    torch.cuda.synchronize(dev)
+    rc = moe.last_device_status(ws)
+    print(json.dumps({"profile_run": cfg.name, "forwards": args.warmup + 1, "device_status": rc}))
+    return 0 if rc == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile", action="store_true",
+                    help="run --warmup forwards, then one more forward, and exit (no timing): "
+                         "the command line for ncu captures")
+    ap.add_argument("--workload", type=int, default=WORKLOAD,
+                    help="with --profile: which workload (1-5) to run")
     args = ap.parse_args()
     world, rank, local = dist_init()
+    if args.profile:
+        return run_profile(args, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)

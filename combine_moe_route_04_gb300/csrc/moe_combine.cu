@@ -6,11 +6,9 @@
 // with a float32 accumulator in slot order, each product and each sum rounded
 // to float32 (__fmul_rn / __fadd_rn keep the compiler from fusing them).
 //
-// One thread per 8 output columns of one token: it gathers the k expert rows
-// of its token with 16-byte loads (all k loads issued before the sums, for
-// memory-level parallelism), so a warp reads 512 contiguous bytes of each
-// expert row and writes 512 contiguous bytes of out.  No atomics: results are
-// bitwise reproducible.
+// One warp per token: a warp reads 512 contiguous bytes of each of the k
+// expert rows per load instruction and writes 512 contiguous bytes of out.
+// No atomics: results are bitwise reproducible.
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -19,72 +17,96 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxK = 16;
-
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y,
+// One warp per token (grid-stride): lanes j < k load the token's row index and
+// weight once and broadcast them; then each lane gathers CH 16-byte chunks of
+// all k expert rows per iteration (k*CH loads in flight per lane) and sums
+// them in slot order.
+template <int KMAX, int CH>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restrict__ Y,
                                                       const int32_t* __restrict__ scatter_idx,
                                                       const float* __restrict__ topk_w, int T, int H, int k,
                                                       int64_t max_rows, uint16_t* __restrict__ out,
                                                       uint32_t* __restrict__ status) {
-  const int vec_per_row = H / 8;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(T) * vec_per_row) return;
-  const int t = static_cast<int>(idx / vec_per_row);
-  const int v = static_cast<int>(idx - static_cast<int64_t>(t) * vec_per_row);
-
-  int64_t rows[kMaxK];
-  float w[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    rows[j] = -1;
-    w[j] = 0.0f;
-    if (j < k) {
-      const int64_t r = __ldg(scatter_idx + static_cast<int64_t>(t) * k + j);
-      w[j] = __ldg(topk_w + static_cast<int64_t>(t) * k + j);
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int vpr = H / 8;  // 16-byte chunks per row
+  for (int64_t t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+      const int64_t r = __ldg(scatter_idx + t * k + lane);
+      my_w = __ldg(topk_w + t * k + lane);
       if (r >= 0 && r < max_rows) {
-        rows[j] = r;
+        my_row = static_cast<int>(r);
       } else if (status != nullptr) {
         record_status(status, kStatusBounds);
       }
     }
-  }
-  uint4 y[kMaxK];
+    int rows[KMAX];
+    float w[KMAX];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    y[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (j < k && rows[j] >= 0) y[j] = __ldg(reinterpret_cast<const uint4*>(Y + rows[j] * H) + v);
-  }
-  float acc[8];
+    for (int j = 0; j < KMAX; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+      w[j] = __shfl_sync(0xffffffffu, my_w, j);
+    }
+    const uint4* Y4 = reinterpret_cast<const uint4*>(Y);
+    uint4* orow = reinterpret_cast<uint4*>(out + t * H);
+    for (int c0 = 0; c0 < vpr; c0 += 32 * CH) {
+      uint4 y[KMAX][CH];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < KMAX; ++j) {
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k) {
-      const uint32_t p[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+        for (int cc = 0; cc < CH; ++cc) {
+          const int v = c0 + cc * 32 + lane;
+          y[j][cc] = make_uint4(0u, 0u, 0u, 0u);
+          if (j < k && rows[j] >= 0 && v < vpr) y[j][cc] = __ldg(Y4 + static_cast<int64_t>(rows[j]) * vpr + v);
+        }
+      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w[j], bf16lo_to_f32(p[i])));
-        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w[j], bf16hi_to_f32(p[i])));
+      for (int cc = 0; cc < CH; ++cc) {
+        const int v = c0 + cc * 32 + lane;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (j < k) {
+            const uint32_t p[4] = {y[j][cc].x, y[j][cc].y, y[j][cc].z, y[j][cc].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w[j], bf16lo_to_f32(p[i])));
+              acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w[j], bf16hi_to_f32(p[i])));
+            }
+          }
+        }
+        if (v < vpr) {
+          uint4 o;
+          o.x = pack_bf16x2(acc[0], acc[1]);
+          o.y = pack_bf16x2(acc[2], acc[3]);
+          o.z = pack_bf16x2(acc[4], acc[5]);
+          o.w = pack_bf16x2(acc[6], acc[7]);
+          orow[v] = o;
+        }
       }
     }
   }
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H)[v] = o;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx, const float* topk_w,
                            uint16_t* out, uint32_t* status, cudaStream_t st) {
-  const int64_t n = static_cast<int64_t>(s.T) * (s.H / 8);
-  const int threads = 256;
-  combine_kernel<<<static_cast<unsigned>((n + threads - 1) / threads), threads, 0, st>>>(
-      Y, scatter_idx, topk_w, s.T, s.H, s.k, max_rows_of(s), out, status);
-  return cudaGetLastError();
+  int64_t blocks = (static_cast<int64_t>(s.T) + 7) / 8;  // 8 warps (tokens) per CTA
+  if (blocks > 4096) blocks = 4096;
+  const int64_t mr = max_rows_of(s);
+  if (s.k <= 8)
+    return launch_pdl(combine_kernel<8, 2>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, Y, scatter_idx,
+                      topk_w, s.T, s.H, s.k, mr, out, status);
+  return launch_pdl(combine_kernel<16, 1>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, Y, scatter_idx,
+                    topk_w, s.T, s.H, s.k, mr, out, status);
 }
 
 }  // namespace moe

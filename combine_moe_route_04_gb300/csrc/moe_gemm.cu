@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -156,6 +157,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // the prologue above overlaps the previous kernel; from here on this
+  // kernel reads what earlier kernels wrote and overwrites what they read
+  pdl_wait();
   int num_blocks = __ldg(num_blocks_ptr);
   if (num_blocks > max_blocks || num_blocks < 0) {
     if (threadIdx.x == 0) record_status(status, kStatusBounds);
@@ -341,6 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ gather_idx,
                                     const int32_t* __restrict__ num_blocks_ptr, int64_t max_rows, int T, int H,
                                     uint16_t* __restrict__ Xp, uint32_t* __restrict__ status) {
+  pdl_launch_dependents();
+  pdl_wait();
   int64_t rows = static_cast<int64_t>(__ldg(num_blocks_ptr)) * BM;
   if (rows > max_rows || rows < 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, kStatusBounds);
@@ -386,10 +392,9 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, const int32_t*
   const int64_t max_tiles = mb * NT;
   const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
   if (grid <= 0) return cudaSuccess;
-  grouped_gemm_kernel<kUp><<<grid, NUM_THREADS, SMEM_ALLOC, st>>>(maps.a, maps.b0, maps.b1, maps.d, off_pad,
-                                                                  block_expert, num_blocks, static_cast<int>(mb),
-                                                                  s.E, K, NT, kUp ? s.I : s.H, status);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<kUp>, dim3(grid), dim3(NUM_THREADS), SMEM_ALLOC, st, maps.a, maps.b0,
+                    maps.b1, maps.d, off_pad, block_expert, num_blocks, static_cast<int>(mb), s.E, K, NT,
+                    kUp ? s.I : s.H, status);
 }
 
 }  // namespace
@@ -400,9 +405,8 @@ cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int
   const int threads = 256;
   int64_t blocks = (mr + 7) / 8;
   if (blocks > 4096) blocks = 4096;
-  permute_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(X, gather_idx, num_blocks, mr, s.T, s.H,
-                                                                        Xp, status);
-  return cudaGetLastError();
+  return launch_pdl(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, X, gather_idx,
+                    num_blocks, mr, s.T, s.H, Xp, status);
 }
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,

@@ -46,6 +46,24 @@ moe_status validate_shape(const moe_shape* s);
 
 inline uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
+// Launch with programmatic stream serialisation (the kernel must call
+// pdl_wait() before touching memory its predecessors use).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Launchers (asynchronous; return cudaGetLastError()).
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
                          int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,

@@ -13,15 +13,16 @@
 //   row of (t, j) = off_pad[e] + #{t' < t routed to e} (stable by token).
 //
 // Kernels:
-//   1. route_topk_hist: one CTA = one chunk of 32 tokens, one warp per token
-//      (warp max / argmax by shuffles); then warp 0 ranks the chunk's T*k
-//      entries with __match_any_sync + popc (stable in-chunk rank per expert)
-//      and writes the chunk's expert histogram.
-//   2. route_scan: one CTA; per expert a warp scans the chunk histograms
-//      (chunk bases), then the padded exclusive scan over experts, the block
-//      table and the -1 fill of padding rows.
-//   3. route_scatter: one thread per (t, j): row = off_pad[e] + chunk base +
-//      in-chunk rank; writes scatter_idx and gather_idx.
+//   1. route_topk_hist: one CTA = one chunk of 32 tokens, one warp per token;
+//      top-k by k rounds of a warp max over packed (logit, index) keys; then
+//      warp 0 ranks the chunk's entries with __match_any_sync + popc (stable
+//      in-chunk rank per expert) and writes the chunk's histogram.
+//   2. route_chunk_scan: one warp per expert scans its chunk histogram (the
+//      chunk bases) and writes the expert's row count.
+//   3. route_scatter: every CTA scans the padded counts (off_pad) in shared
+//      memory; one thread per (t, j) writes row = off_pad[e] + chunk base +
+//      in-chunk rank to scatter_idx and gather_idx; the block table and the
+//      padding rows' -1 are spread over all threads.
 // Integer atomics are not used, so every output is a pure function of the
 // logits.
 #include <cfloat>
@@ -37,12 +38,7 @@ namespace {
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kMaxEPerLane = kMaxE / 32;
-
-struct Cand {
-  float v;   // logit
-  int e;     // expert index
-  float x;   // exp(logit - max)
-};
+constexpr int kTopkThreads = 32 * kChunkTokens;              // one warp per token of the chunk
 
 // exp(v - m) for float32 v <= m: the difference is split exactly into
 // d_hi + d_lo (2Sum) and exp(d_hi + d_lo) ~= exp(d_hi) * (1 + d_lo), so the
@@ -56,18 +52,34 @@ __device__ __forceinline__ float exp_diff(float v, float m) {
   return fmaf(e, d_lo, e);
 }
 
-__device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
-  return va > vb || (va == vb && ea < eb);
+// Sort key of (logit, expert): the logit's bits mapped to an unsigned order
+// (after -0 -> +0, so the two zeros tie as they compare equal) in the high
+// word and 0xFFFF - e in the low word: a larger key is a larger logit, or an
+// equal logit with a lower index.  0 is below every real key.
+__device__ __forceinline__ uint64_t pick_key(float v, int e) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(0xFFFF - e);
 }
+__device__ __forceinline__ float key_logit(uint64_t key) {
+  const uint32_t ord = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+__device__ __forceinline__ int key_expert(uint64_t key) { return 0xFFFF - static_cast<int>(key & 0xFFFFu); }
 
-__global__ void __launch_bounds__(1024) route_topk_hist_kernel(const float* __restrict__ logits, int T, int E,
-                                                               int k, int nch, int32_t* __restrict__ topk_ids,
-                                                               float* __restrict__ topk_w,
-                                                               int32_t* __restrict__ local_rank,
-                                                               int32_t* __restrict__ chunk_counts) {
+// Kernel 1: one CTA per chunk of 32 tokens, one warp per token: the k best
+// experts (k rounds of a warp-wide max over the keys, the winner removed
+// each round; slot j = j-th round) and the renormalised weights; then warp 0
+// forms the chunk's expert histogram and each entry's stable in-chunk rank.
+// EPL = logits per lane (E <= 32 * EPL).
+template <int EPL>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int nch, int32_t* __restrict__ topk_ids,
+    float* __restrict__ topk_w, int32_t* __restrict__ local_rank, int32_t* __restrict__ chunk_counts) {
   __shared__ int32_t s_ids[kChunkTokens * kMaxK];
   __shared__ int32_t s_cnt[kMaxE];
 
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
@@ -75,71 +87,58 @@ __global__ void __launch_bounds__(1024) route_topk_hist_kernel(const float* __re
   const int ntok = min(kChunkTokens, T - t0);
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  pdl_wait();  // inputs and outputs may be in use by the previous kernel until here
 
   if (warp < ntok) {
     const int t = t0 + warp;
     const float* row = logits + static_cast<int64_t>(t) * E;
-    float v[kMaxEPerLane];
-    float x[kMaxEPerLane];
-    float m = -FLT_MAX;
+    uint64_t key[EPL];
 #pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) {
+    for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? __ldg(row + e) : -FLT_MAX;
-      if (e < E) m = fmaxf(m, v[i]);
+      key[i] = (e < E) ? pick_key(__ldg(row + e), e) : 0ull;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-#pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) x[i] = (lane + 32 * i < E) ? exp_diff(v[i], m) : 0.0f;
-
-    uint32_t taken = 0;  // bit i: element i of this lane already picked
-    int my_id = 0;
-    float my_x = 0.0f;
+    uint64_t my_key = 0;
     for (int j = 0; j < k; ++j) {
-      // best unpicked element of this lane (ascending index: strict > keeps the lower)
-      Cand c{-INFINITY, 0x7fffffff, 0.0f};
+      uint64_t best = key[0];
 #pragma unroll
-      for (int i = 0; i < kMaxEPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && better(v[i], e, c.v, c.e)) c = Cand{v[i], e, x[i]};
-      }
-      // warp argmax, ties to the lower index
+      for (int i = 1; i < EPL; ++i) best = key[i] > best ? key[i] : best;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, c.v, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, c.e, o);
-        const float ox = __shfl_xor_sync(0xffffffffu, c.x, o);
-        if (better(ov, oe, c.v, c.e)) c = Cand{ov, oe, ox};
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
       }
-      if ((c.e & 31) == lane) taken |= 1u << (c.e >> 5);
-      if (lane == j) {
-        my_id = c.e;
-        my_x = c.x;
-      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) key[i] = (key[i] == best) ? 0ull : key[i];  // keys are unique
+      if (lane == j) my_key = best;
     }
-    // renormalise over the picks: w_j = x_j / sum_{j' in slot order} x_j'
-    // (the softmax denominator cancels).  Slots hold non-increasing x, so
-    // Fast2Sum keeps the rounding error of each addition.
+    // the first pick is the row maximum
+    const float m = key_logit(__shfl_sync(0xffffffffu, my_key, 0));
+    const int my_e = key_expert(my_key);
+    const float my_x = (lane < k) ? exp_diff(key_logit(my_key), m) : 0.0f;
+    // w_j = x_j / sum_{j' in slot order} x_j' (the softmax denominator
+    // cancels); slots hold non-increasing x, so Fast2Sum keeps the rounding
+    // error of each addition
     float S = 0.0f, comp = 0.0f;
     for (int j = 0; j < k; ++j) {
       const float y = __shfl_sync(0xffffffffu, my_x, j);
-      const float t = S + y;
-      comp += (S - t) + y;
-      S = t;
+      const float tt = S + y;
+      comp += (S - tt) + y;
+      S = tt;
     }
     S += comp;
     if (lane < k) {
-      topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
+      topk_ids[static_cast<int64_t>(t) * k + lane] = my_e;
       topk_w[static_cast<int64_t>(t) * k + lane] = my_x / S;
-      s_ids[warp * k + lane] = my_id;
+      s_ids[warp * k + lane] = my_e;
     }
   }
   __syncthreads();
 
   if (warp == 0) {
     // stable rank of every (t, j) of the chunk among the chunk's entries of
-    // the same expert, entries in (t, j) order
+    // the same expert, entries in (t, j) order: one batch of 32 entries at a
+    // time, peers with the same expert found by __match_any_sync
     const int n = ntok * k;
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (int base = 0; base < n; base += 32) {
@@ -159,83 +158,102 @@ __global__ void __launch_bounds__(1024) route_topk_hist_kernel(const float* __re
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[static_cast<int64_t>(e) * nch + chunk] = s_cnt[e];
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nch, int64_t max_blocks,
-                                                          int32_t* __restrict__ chunk_counts,
-                                                          int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ off_pad,
-                                                          int32_t* __restrict__ block_expert,
-                                                          int32_t* __restrict__ num_blocks,
-                                                          int32_t* __restrict__ gather_idx,
-                                                          uint32_t* __restrict__ status) {
-  __shared__ int32_t s_cnt[kMaxE];
-  __shared__ int32_t s_off[kMaxE + 1];
-  const int warp = threadIdx.x >> 5;
+// Kernel 2: one warp per expert: exclusive scan of its chunk histogram (the
+// chunk bases, in place) and its total row count.
+__global__ void __launch_bounds__(256) route_chunk_scan_kernel(int E, int nch, int32_t* __restrict__ chunk_counts,
+                                                               int32_t* __restrict__ counts) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-
-  // per expert: exclusive scan of the chunk histograms -> chunk bases
-  for (int e = warp; e < E; e += nwarps) {
-    int32_t* cc = chunk_counts + static_cast<int64_t>(e) * nch;
-    int running = 0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = (c < nch) ? cc[c] : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (c < nch) cc[c] = running + incl - v;
-      running += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s_cnt[e] = running;
-      counts[e] = running;
-    }
-  }
-  __syncthreads();
-
-  // exclusive scan over experts of the 128-padded counts
-  if (warp == 0) {
-    constexpr int per = kMaxE / 32;
-    int local[per];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      local[i] = (e < E) ? (s_cnt[e] + kRowBlock - 1) / kRowBlock * kRowBlock : 0;
-      sum += local[i];
-    }
-    int incl = sum;
+  if (e >= E) return;
+  int32_t* cc = chunk_counts + static_cast<int64_t>(e) * nch;
+  int running = 0;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = (c < nch) ? cc[c] : 0;
+    int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    int run = incl - sum;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E) s_off[e] = run;
-      run += local[i];
-    }
-    if (lane == 31) s_off[E] = incl;
+    if (c < nch) cc[c] = running + incl - v;
+    running += __shfl_sync(0xffffffffu, incl, 31);
   }
+  if (lane == 0) counts[e] = running;
+}
+
+// Kernel 3: every CTA forms off_pad (exclusive scan of the 128-padded counts)
+// in shared memory, then one thread per (t, j) writes its permuted row; the
+// block table and the padding rows' -1 are spread over all threads.
+__global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, int nch, int64_t max_blocks,
+                                                            const int32_t* __restrict__ topk_ids,
+                                                            const int32_t* __restrict__ counts,
+                                                            const int32_t* __restrict__ chunk_base,
+                                                            int32_t* __restrict__ scatter_idx,  // in: rank, out: row
+                                                            int32_t* __restrict__ gather_idx,
+                                                            int32_t* __restrict__ off_pad,
+                                                            int32_t* __restrict__ block_expert,
+                                                            int32_t* __restrict__ num_blocks,
+                                                            uint32_t* __restrict__ status) {
+  __shared__ int32_t s_off[kMaxE + 1];
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_warp[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  // block-wide exclusive scan of padded counts (E <= 256 = blockDim.x)
+  const int c = (tid < E) ? __ldg(counts + tid) : 0;
+  if (tid < E) s_cnt[tid] = c;
+  const int padded = (c + kRowBlock - 1) / kRowBlock * kRowBlock;
+  int incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_warp[w];
+  if (tid < E) s_off[tid] = wbase + incl - padded;
+  if (tid == E - 1) s_off[E] = wbase + incl;
   __syncthreads();
 
-  const int total_rows = s_off[E];
-  int nb = total_rows / kRowBlock;
+  int nb = s_off[E] / kRowBlock;
   if (nb > max_blocks) {  // impossible for valid expert ids; keep every later index in range
-    if (threadIdx.x == 0) record_status(status, kStatusBounds);
+    if (tid == 0 && blockIdx.x == 0) record_status(status, kStatusBounds);
     nb = static_cast<int>(max_blocks);
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off_pad[e] = s_off[e];
-  if (threadIdx.x == 0) *num_blocks = nb;
-
-  // block table: expert whose padded range holds row 128*b
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    const int row = b * kRowBlock;
+  const int64_t max_rows = max_blocks * kRowBlock;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (blockIdx.x == 0) {
+    for (int e = tid; e <= E; e += blockDim.x) off_pad[e] = s_off[e];
+    if (tid == 0) *num_blocks = nb;
+  }
+  // entries
+  for (int64_t i = gtid; i < static_cast<int64_t>(T) * k; i += nthreads) {
+    const int t = static_cast<int>(i / k);
+    const int e = topk_ids[i];
+    if (e < 0 || e >= E) {
+      record_status(status, kStatusBounds);
+      continue;
+    }
+    const int64_t row = static_cast<int64_t>(s_off[e]) +
+                        chunk_base[static_cast<int64_t>(e) * nch + t / kChunkTokens] + scatter_idx[i];
+    if (row < 0 || row >= max_rows) {
+      record_status(status, kStatusBounds);
+      continue;
+    }
+    scatter_idx[i] = static_cast<int32_t>(row);
+    gather_idx[row] = t;
+  }
+  // block table: the expert whose padded range holds row 128*b
+  for (int64_t b = gtid; b < nb; b += nthreads) {
+    const int row = static_cast<int>(b) * kRowBlock;
     int lo = 0, hi = E - 1;  // smallest e with s_off[e+1] > row
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -243,36 +261,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, int nch, int64_
     }
     block_expert[b] = lo;
   }
-  // padding rows of every expert
-  for (int e = warp; e < E; e += nwarps) {
-    const int end = min(s_off[e + 1], nb * kRowBlock);
-    for (int r = s_off[e] + s_cnt[e] + lane; r < end; r += 32) gather_idx[r] = -1;
+  // padding rows of every expert: (e, p) -> row off_pad[e] + counts[e] + p
+  for (int64_t g = gtid; g < static_cast<int64_t>(E) * kRowBlock; g += nthreads) {
+    const int e = static_cast<int>(g / kRowBlock);
+    const int64_t row = static_cast<int64_t>(s_off[e]) + s_cnt[e] + (g % kRowBlock);
+    if (row < s_off[e + 1] && row < static_cast<int64_t>(nb) * kRowBlock) gather_idx[row] = -1;
   }
-}
-
-__global__ void route_scatter_kernel(int T, int E, int k, int nch, int64_t max_rows,
-                                     const int32_t* __restrict__ topk_ids,
-                                     const int32_t* __restrict__ off_pad,
-                                     const int32_t* __restrict__ chunk_base,
-                                     int32_t* __restrict__ scatter_idx,  // in: in-chunk rank, out: row
-                                     int32_t* __restrict__ gather_idx, uint32_t* __restrict__ status) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<int64_t>(T) * k) return;
-  const int t = static_cast<int>(i / k);
-  const int e = topk_ids[i];
-  if (e < 0 || e >= E) {
-    record_status(status, kStatusBounds);
-    return;
-  }
-  const int chunk = t / kChunkTokens;
-  const int64_t row =
-      static_cast<int64_t>(off_pad[e]) + chunk_base[static_cast<int64_t>(e) * nch + chunk] + scatter_idx[i];
-  if (row < 0 || row >= max_rows) {
-    record_status(status, kStatusBounds);
-    return;
-  }
-  scatter_idx[i] = static_cast<int32_t>(row);
-  gather_idx[row] = t;
 }
 
 }  // namespace
@@ -282,14 +276,26 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
                          int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts, uint32_t* status,
                          cudaStream_t st) {
   const int nch = static_cast<int>(num_chunks_of(s));
-  route_topk_hist_kernel<<<nch, 1024, 0, st>>>(logits, s.T, s.E, s.k, nch, topk_ids, topk_w, scatter_idx,
-                                                chunk_counts);
-  route_scan_kernel<<<1, 1024, 0, st>>>(s.E, nch, max_blocks_of(s), chunk_counts, counts, off_pad, block_expert,
-                                        num_blocks, gather_idx, status);
+  cudaError_t err;
+  const int epl = (s.E + 31) / 32;
+  auto k1 = epl <= 1 ? route_topk_hist_kernel<1>
+          : epl <= 2 ? route_topk_hist_kernel<2>
+          : epl <= 4 ? route_topk_hist_kernel<4>
+                     : route_topk_hist_kernel<8>;
+  err = launch_pdl(k1, dim3(nch), dim3(kTopkThreads), 0, st, logits, s.T, s.E, s.k, nch, topk_ids, topk_w,
+                   scatter_idx, chunk_counts);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(route_chunk_scan_kernel, dim3((s.E + 7) / 8), dim3(256), 0, st, s.E, nch, chunk_counts, counts);
+  if (err != cudaSuccess) return err;
   const int64_t n = static_cast<int64_t>(s.T) * s.k;
-  const int threads = 256;
-  route_scatter_kernel<<<static_cast<unsigned>((n + threads - 1) / threads), threads, 0, st>>>(
-      s.T, s.E, s.k, nch, max_rows_of(s), topk_ids, off_pad, chunk_counts, scatter_idx, gather_idx, status);
+  const int64_t work = n > static_cast<int64_t>(s.E) * kRowBlock ? n : static_cast<int64_t>(s.E) * kRowBlock;
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > 1184) blocks = 1184;
+  err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.E, s.k, nch,
+                   static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
+                   static_cast<const int32_t*>(counts), static_cast<const int32_t*>(chunk_counts), scatter_idx,
+                   gather_idx, off_pad, block_expert, num_blocks, status);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
