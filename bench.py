@@ -389,6 +389,9 @@ def run_profile(args, local):
     dev = torch.device("cuda", local)
     _build.build()
     cfg = moe_inputs.config(args.workload)
+    if args.shape:
+        T, H, I, E, k = (int(v) for v in args.shape.split(","))
+        cfg = moe_inputs.MoEConfig("shape_%d_%d_%d_%d_%d" % (T, H, I, E, k), T, H, I, E, k, seed=7)
     inp = moe_inputs.make_inputs(cfg)
     s = moe.shape(*cfg.shape)
 
@@ -418,6 +421,8 @@ def main():
                          "the command line for ncu captures")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
                     help="with --profile: which workload (1-5) to run")
+    ap.add_argument("--shape", type=str, default=None,
+                    help="with --profile: T,H,I,E,k of a synthetic shape instead of a workload")
     args = ap.parse_args()
     world, rank, local = dist_init()
     if args.profile:

@@ -115,8 +115,8 @@ moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_i
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
-  if (!encode_bf16_2d(&m.a, w.xp, mr, s.H, 128, 64) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 64, 64) ||
-      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 64, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
+  if (!encode_bf16_2d(&m.a, w.xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
+      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
     return MOE_ERR_CUDA;
   return cuda_status(launch_gemm_up(s, m, off_pad, block_expert, num_blocks, w.status, num_sms, st));
 }
@@ -127,7 +127,7 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* off_pa
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EI = static_cast<uint64_t>(s.E) * s.I;
-  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 64) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 64, 64) ||
+  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64) ||
       !encode_bf16_2d(&m.d, Y, mr, s.H, 128, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
@@ -175,9 +175,12 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                     : CU_TENSOR_MAP_SWIZZLE_NONE;
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

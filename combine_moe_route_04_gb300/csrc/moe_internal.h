@@ -7,7 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -74,10 +74,10 @@ cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int
                                 const int32_t* num_blocks, uint16_t* Xp, uint32_t* status, cudaStream_t st);
 
 struct GemmMaps {
-  CUtensorMap a;     // A operand rows (K-major): Xp [max_rows][H] or h [max_rows][I]
-  CUtensorMap b0;    // up: W_gate [E*H][I]; down: W_down [E*I][H]
+  CUtensorMap a;     // A operand rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32
+  CUtensorMap b0;    // up: W_gate [E*H][I]; down: W_down [E*I][H]; box 32 x 64
   CUtensorMap b1;    // up: W_up   [E*H][I]; down: unused (copy of b0)
-  CUtensorMap d;     // output rows: h [max_rows][I] or Y [max_rows][H]
+  CUtensorMap d;     // output rows: h [max_rows][I] or Y [max_rows][H]; box 128 x 64
 };
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
@@ -91,7 +91,8 @@ cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t*
                            const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda).
-// rows x cols bf16 row-major, box = box_cols (inner) x box_rows, 128-byte swizzle.
+// rows x cols bf16 row-major, box = box_cols (inner) x box_rows; the swizzle
+// span equals the box's inner extent in bytes (64 or 128).
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                     uint32_t box_cols);
 
