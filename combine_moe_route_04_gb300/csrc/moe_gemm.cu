@@ -12,28 +12,29 @@
 //   down: Y[b, j] = bf16(h_b Wd[e][:, j]) for 256-column slices j.
 //
 // Design (the roles and barrier lifetimes of "TIRx 与高性能GEMM (下)" Step 7,
-// re-keyed to expert blocks; the B-tile sharing of its Step 9 done inside one
-// CTA):
-//   * a tile is a PAIR of 128-row blocks of the same expert (the second may be
-//     absent) times one 256-column MMA tile: both blocks multiply the same B
-//     tile, which cuts the bytes each SM must load per MMA clock by a third;
-//   * warp 0, TMA producer: per 32-deep K stage, A of each block (128x32,
-//     64-byte swizzle) and B (32x256 as four 32x64 boxes, N-major, 128-byte
-//     swizzle) into a 6-stage SMEM ring guarded by full/empty mbarriers;
-//   * warp 1 allocates all 512 TMEM columns (accumulator 0 = block 0 and
-//     accumulator 1 = block 1, 128x256 f32 each) and one elected lane issues
-//     tcgen05.mma M=128 N=256 K=16 into each accumulator, committing SMEM
-//     stages back to the producer and finished accumulators to the epilogue;
-//   * warps 2-5 drain accumulator 0 and warps 6-9 accumulator 1 (thread =
-//     row): tcgen05.ld, SiLU*up or bf16 cast, all into registers, then the
-//     TMEM is released at once so the next tile's MMAs start while the rows
-//     go out through a swizzled SMEM box and TMA stores;
+// and the two-CTA MMA of its Step 8, re-keyed to expert blocks):
+//   * a tile is a PAIR of 128-row blocks of the same expert times one
+//     256-column MMA tile, computed by a cluster of two CTAs on two SMs with
+//     M=256 tcgen05.mma (cta_group::2): CTA r owns block b0 + r (its A rows,
+//     its 128 accumulator rows in its own TMEM) and half of the B tile;
+//   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its A (128x32,
+//     64-byte swizzle) and its B half (32x128 as two 32x64 boxes, N-major,
+//     128-byte swizzle) into a 12-stage SMEM ring; all loads complete on CTA
+//     0's full barriers;
+//   * warp 1 allocates 512 TMEM columns in both CTAs (two 128x256 f32
+//     accumulators each); in CTA 0 one elected lane issues the MMAs and
+//     commits stages back to both producers and finished accumulators to
+//     both epilogues;
+//   * warps 2-5 of each CTA drain the accumulator (thread = row) into
+//     registers (SiLU*up or bf16 cast), release it on CTA 0's
+//     accumulator-empty barrier so the next tile's MMAs overlap this
+//     writeback, and store the rows through a swizzled SMEM box and TMA;
 //   * tile order: expert by expert; inside an expert, groups of GROUP_PAIRS
 //     pairs, all column tiles of a group before the next group, so the
 //     group's A rows stay in L2 while every B tile of the expert streams by.
-// Every wait is bounded; on a timeout the kernel records it in the status
-// word, the roles stop, in-flight copies and MMAs are drained (bounded) and
-// TMEM is freed before exit.
+// Every wait on an mbarrier is bounded; on a timeout the kernel records it in
+// the status word, the roles stop, in-flight copies and MMAs are drained
+// (bounded) and TMEM is freed before exit.
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -45,45 +46,14 @@ namespace {
 constexpr int BM = 128;                          // rows per block
 constexpr int BK = 32;                           // K per pipeline stage
 constexpr int BN = 256;                          // MMA N
-constexpr int STAGES = 6;
 constexpr int GROUP_PAIRS = 4;                   // L2 grouping of pairs inside an expert
 constexpr int A_BLOCK_BYTES = BM * BK * 2;       // 8 KB: 128 rows x 64 B (64-byte swizzle)
 constexpr int B_BOX_BYTES = BK * 64 * 2;         // 4 KB: 32 k-rows x 64 columns (128-byte swizzle)
-constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;   // 16 KB
-constexpr int STAGE_BYTES = 2 * A_BLOCK_BYTES + B_STAGE_BYTES;  // 32 KB
 constexpr int EPI_BOX_BYTES = BM * 64 * 2;       // 16 KB: 128 rows x 64 columns bf16
-constexpr int NUM_EPI_GROUPS = 2;
-constexpr int EPI_THREADS = 128;                 // per group
-constexpr int NUM_THREADS = 64 + NUM_EPI_GROUPS * EPI_THREADS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
 
-constexpr int SMEM_STAGE_OFF = 0;
-constexpr int SMEM_EPI_OFF = STAGES * STAGE_BYTES;
-constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + NUM_EPI_GROUPS * EPI_BOX_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 1 + 2 + 1;  // full, empty, tmem_full, tmem_empty[2], drain
-constexpr int SMEM_PAIR_OFF = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int MAX_E = 256;
-constexpr int SMEM_BYTES = SMEM_PAIR_OFF + (MAX_E + 1) * 4;
-constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;   // slack to align the base to 1024 B
-
-static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, 256, /*b_mn_major=*/true);
-
-// OR-vote over the 128 threads of epilogue group g (named barrier 2 + 2g).
-__device__ __forceinline__ bool vote_any_group(bool flag, int g) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, 128, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(flag ? 1u : 0u), "r"(2 + 2 * g)
-      : "memory");
-  return r != 0;
-}
 
 struct TileCoord {
   int b0;     // first block of the pair
@@ -123,38 +93,81 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, int NT, int E, int nu
   return c;
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant: a cluster of two CTAs on two SMs computes one 256-row x
+// 256-column tile with M=256 MMAs (cta_group::2): CTA r holds block b0 + r of
+// the pair (128 rows of A, 128 rows of the accumulator in its own TMEM) and
+// HALF of the 256-column B tile (up: CTA 0 the gate columns, CTA 1 the up
+// columns; down: the lower / upper 128 columns).  Per SM, each stage moves
+// 8 KB of A and 8 KB of B and the tensor core reads its half of B once for
+// both SMs, which halves the shared-memory traffic per MMA of the single-CTA
+// kernel; the accumulator is 256 TMEM columns per CTA, so two accumulators
+// double-buffer the epilogue against the next tile's MMAs.  CTA 0 issues the
+// MMAs; both CTAs' loads complete on CTA 0's full barriers; its commits
+// arrive on both CTAs' empty / accumulator-full barriers; both CTAs' epilogue
+// warps release the accumulator on CTA 0's accumulator-empty barrier.  When
+// the pair has only one block, CTA 1 loads block b0's rows again and stores
+// nothing.
+constexpr int P_STAGES = 12;
+constexpr int P_B_HALF_BYTES = 2 * B_BOX_BYTES;                 // 8 KB: 32 k-rows x 128 columns
+constexpr int P_STAGE_BYTES = A_BLOCK_BYTES + P_B_HALF_BYTES;   // 16 KB
+constexpr int P_THREADS = 192;                                  // producer, MMA, 4 epilogue warps
+constexpr int P_SMEM_EPI_OFF = P_STAGES * P_STAGE_BYTES;
+constexpr int P_SMEM_BAR_OFF = P_SMEM_EPI_OFF + 2 * EPI_BOX_BYTES;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 2 + 2 + 1;           // full, empty, tmem_full[2], tmem_empty[2], drain
+constexpr int P_SMEM_PAIR_OFF = P_SMEM_BAR_OFF + P_NUM_BARS * 8 + 16;
+constexpr int P_SMEM_BYTES = P_SMEM_PAIR_OFF + (MAX_E + 1) * 4;
+constexpr int P_SMEM_ALLOC = P_SMEM_BYTES + 1024;
+static_assert(P_SMEM_ALLOC <= 232448, "shared memory budget (pair kernel)");
+constexpr uint32_t kIdescPair = idesc_bf16_f32(256, 256, /*b_mn_major=*/true);
+
+__device__ __forceinline__ bool vote_any_epi(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 2, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(flag ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 template <bool kUp>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmD,
-                        const int32_t* __restrict__ off_pad, const int32_t* __restrict__ num_blocks_ptr,
-                        int max_blocks, int E, int K, int NT, int N_out, uint32_t* __restrict__ status) {
+__global__ void __launch_bounds__(P_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmD,
+                             const int32_t* __restrict__ off_pad, const int32_t* __restrict__ num_blocks_ptr,
+                             int max_blocks, int E, int K, int NT, int N_out, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sStage = smem + SMEM_STAGE_OFF;
-  uint8_t* sEpi = smem + SMEM_EPI_OFF;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR_OFF);
+  uint8_t* sStage = smem;
+  uint8_t* sEpi = smem + P_SMEM_EPI_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_SMEM_BAR_OFF);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 1;
-  uint64_t* drain = bars + 2 * STAGES + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  uint64_t* empty = bars + P_STAGES;
+  uint64_t* tfull = bars + 2 * P_STAGES;
+  uint64_t* tempty = bars + 2 * P_STAGES + 2;
+  uint64_t* drain = bars + 2 * P_STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_pair_off = reinterpret_cast<int32_t*>(smem + SMEM_PAIR_OFF);
+  int32_t* s_pair_off = reinterpret_cast<int32_t*>(smem + P_SMEM_PAIR_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(&tempty[0], EPI_THREADS);
-    mbar_init(&tempty[1], EPI_THREADS);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * 4);  // one arrival per epilogue warp of both CTAs
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -163,13 +176,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmB1);
     prefetch_tmap(&tmD);
   }
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
 
-  // the prologue above overlaps the previous kernel; from here on this
-  // kernel reads what earlier kernels wrote and overwrites what they read
   pdl_wait();
   int num_blocks = __ldg(num_blocks_ptr);
   if (num_blocks > max_blocks || num_blocks < 0) {
@@ -177,7 +189,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     num_blocks = num_blocks < 0 ? 0 : max_blocks;
   }
   if (warp == 2) {
-    // pairs per expert -> exclusive scan (E <= 256: 8 experts per lane)
     constexpr int per = MAX_E / 32;
     int loc[per];
     int sum = 0;
@@ -202,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e <= E) s_pair_off[e] = run;  // e == E gets the total (loc of e >= E is 0)
+      if (e <= E) s_pair_off[e] = run;
       run += loc[i];
     }
     if (lane == 31 && 32 * per == E) s_pair_off[E] = incl;
@@ -213,182 +224,156 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = NT * s_pair_off[E];
   const int KB = K / BK;
+  const int cluster_id = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const uint32_t full0 = map_to_cta(full, 0);      // CTA 0's full barriers (shared::cluster)
+  const uint32_t tempty0 = map_to_cta(tempty, 0);  // CTA 0's accumulator-empty barriers
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------------------ TMA producer (both CTAs)
     if (elect_one_sync()) {
       const uint64_t pol_a = policy_evict_last();
       const uint64_t pol_b = policy_evict_normal();
-      uint32_t it = 0;  // stages issued so far
+      const CUtensorMap* mapB = (kUp && rank == 1) ? &tmB1 : &tmB0;
+      uint32_t it = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < total_tiles && !stop; tile += gridDim.x) {
+      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
         const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
         if (!c.ok) {
           record_status(status, kStatusBounds);
           continue;
         }
-        const uint32_t bytes = STAGE_BYTES - (c.two ? 0 : A_BLOCK_BYTES);
+        const int my_b = c.b0 + ((rank == 1 && c.two) ? 1 : 0);
+        const int n0 = kUp ? c.j * 128 : c.j * BN + 128 * static_cast<int>(rank);
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
+          const uint32_t s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
             stop = true;
             break;
           }
-          uint8_t* st = sStage + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(st, &tmA, &full[s], kb * BK, c.b0 * BM, pol_a);
-          if (c.two) tma_load_2d(st + A_BLOCK_BYTES, &tmA, &full[s], kb * BK, (c.b0 + 1) * BM, pol_a);
-          uint8_t* b = st + 2 * A_BLOCK_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P_STAGE_BYTES);
+          uint8_t* st = sStage + s * P_STAGE_BYTES;
+          const uint32_t fb = full0 + 8u * s;
           const int k0 = c.e * K + kb * BK;
-          if (kUp) {
-            const int n0 = c.j * 128;
-            tma_load_2d(b + 0 * B_BOX_BYTES, &tmB0, &full[s], n0, k0, pol_b);
-            tma_load_2d(b + 1 * B_BOX_BYTES, &tmB0, &full[s], n0 + 64, k0, pol_b);
-            tma_load_2d(b + 2 * B_BOX_BYTES, &tmB1, &full[s], n0, k0, pol_b);
-            tma_load_2d(b + 3 * B_BOX_BYTES, &tmB1, &full[s], n0 + 64, k0, pol_b);
-          } else {
-            const int n0 = c.j * BN;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tma_load_2d(b + q * B_BOX_BYTES, &tmB0, &full[s], n0 + 64 * q, k0, pol_b);
-          }
+          tma_load_2d_pair(st, &tmA, fb, kb * BK, my_b * BM, pol_a);
+          tma_load_2d_pair(st + A_BLOCK_BYTES, mapB, fb, n0, k0, pol_b);
+          tma_load_2d_pair(st + A_BLOCK_BYTES + B_BOX_BYTES, mapB, fb, n0 + 64, k0, pol_b);
         }
       }
-      // drain: every issued stage's copy has landed before the CTA may exit
-      const uint32_t nst = it < STAGES ? it : STAGES;
+      // drain: every issued stage was consumed by the MMAs (so its copies landed)
+      const uint32_t nst = it < P_STAGES ? it : P_STAGES;
       for (uint32_t s = 0; s < nst; ++s) {
-        const uint32_t last = s + STAGES * ((it - 1 - s) / STAGES);
+        const uint32_t last = s + P_STAGES * ((it - 1 - s) / P_STAGES);
         int no_abort = 0;
-        mbar_wait(&full[s], (last / STAGES) & 1u, &no_abort, status);
+        mbar_wait(&empty[s], (last / P_STAGES) & 1u, &no_abort, status);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
-    if (elect_one_sync()) {
+    // ------------------------------------------------------ MMA issuer (CTA 0)
+    if (rank == 0 && elect_one_sync()) {
       uint32_t it = 0;
-      uint32_t tcount = 0;  // tiles processed by this CTA
+      uint32_t tcount = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < total_tiles && !stop; tile += gridDim.x) {
+      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
         const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
         if (!c.ok) continue;
-        const uint32_t tph = tcount & 1u;
-        // accumulator 0 must be drained before the first MMA; accumulator 1
-        // is waited for after the first stage's accumulator-0 MMAs
-        if (!mbar_wait(&tempty[0], tph ^ 1u, abort_flag, status)) break;
+        const uint32_t a = tcount & 1u;
+        const uint32_t aph = (tcount >> 1) & 1u;
+        if (!mbar_wait(&tempty[a], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
+        const uint32_t d = tmem_base + a * ACC_COLS;
         for (int kb = 0; kb < KB; ++kb, ++it) {
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
+          const uint32_t s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1u;
           if (!mbar_wait(&full[s], ph, abort_flag, status)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(sStage + s * STAGE_BYTES);
-          const uint32_t b_base = st + 2 * A_BLOCK_BYTES;
+          const uint32_t st = smem_u32(sStage + s * P_STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: K-major, 64-byte swizzle, 8-row groups 512 B apart; a
-            //    16-wide K step is 32 B inside the swizzle atom.
-            // B: N-major, 128-byte swizzle; 64-column boxes 4 KB apart
-            //    (leading offset), 8-row K groups 1 KB apart (stride
-            //    offset); a 16-wide K step is two groups.
-            const uint64_t bdesc = smem_desc(b_base + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B);
-            tc_mma_f16(tmem_base, smem_desc(st + kk * 32, 16, 512, kSwizzle64B), bdesc, kIdesc,
-                       (kb | kk) != 0 ? 1u : 0u);
+            // A (each CTA's 128 rows): K-major, 64-byte swizzle, 8-row groups
+            // 512 B apart, 16-wide K step = 32 B.  B (each CTA's 128
+            // columns): N-major, 128-byte swizzle, 64-column boxes 4 KB apart,
+            // 8-row K groups 1 KB apart, 16-wide K step = 2 KB.
+            tc_mma_f16_pair(d, smem_desc(st + kk * 32, 16, 512, kSwizzle64B),
+                            smem_desc(st + A_BLOCK_BYTES + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B), kIdescPair,
+                            (kb | kk) != 0 ? 1u : 0u);
           }
-          if (kb == 0) {
-            if (!mbar_wait(&tempty[1], tph ^ 1u, abort_flag, status)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-          }
-          if (c.two) {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t bdesc = smem_desc(b_base + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B);
-              tc_mma_f16(tmem_base + ACC_COLS, smem_desc(st + A_BLOCK_BYTES + kk * 32, 16, 512, kSwizzle64B),
-                         bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-            }
-          }
-          tc_commit(&empty[s]);
+          tc_commit_pair(&empty[s], 0x3);
         }
         if (stop) break;
-        tc_commit(tfull);
+        tc_commit_pair(&tfull[a], 0x3);
         ++tcount;
       }
-      // drain: all issued MMAs complete before TMEM is freed
-      tc_commit(drain);
+      tc_commit_pair(drain, 0x1);
       int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, status);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------ epilogue
-    const int g = (warp - 2) >> 2;            // accumulator (= block of the pair) of this group
-    const int et = (threadIdx.x - 64) & 127;  // thread index inside the group
-    const int q = warp & 3;                   // TMEM lane quarter of this warp
-    const int r = q * 32 + lane;              // row of the block owned by this thread
-    const uint32_t sync_id = 1 + 2 * g;
-    uint8_t* buf = sEpi + g * EPI_BOX_BYTES;
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int et = threadIdx.x - 64;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
     uint32_t tcount = 0;
-    constexpr int NPACK = kUp ? 64 : 128;     // packed bf16 pairs per row of the tile
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    uint32_t nstore = 0;
+    constexpr int NPACK = kUp ? 64 : 128;
+    for (int tile = cluster_id; tile < total_tiles; tile += nclusters) {
       const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
       if (!c.ok) continue;
-      const bool ok = mbar_wait(tfull, tcount & 1u, abort_flag, status);
-      if (vote_any_group(!ok, g)) break;
+      const uint32_t a = tcount & 1u;
+      const uint32_t aph = (tcount >> 1) & 1u;
+      const bool ok = mbar_wait(&tfull[a], aph, abort_flag, status);
+      if (vote_any_epi(!ok)) break;
       tc_fence_after();
-      const bool mine = (g == 0) || c.two;
       uint32_t packed[NPACK];
-      if (mine) {
-        const uint32_t tbase = tmem_base + g * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-        if (kUp) {
+      const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+      if (kUp) {
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t gv[32], uv[32];
-            tmem_ld_32x32b_x32(tbase + ch * 32, gv);
-            tmem_ld_32x32b_x32(tbase + 128 + ch * 32, uv);
-            tmem_ld_wait();
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t gv[32], uv[32];
+          tmem_ld_32x32b_x32(tbase + ch * 32, gv);
+          tmem_ld_32x32b_x32(tbase + 128 + ch * 32, uv);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-              const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-              // silu(g) = g * sigmoid(g); exp and reciprocal at the SFU's
-              // approximate precision (a few float32 ulps, far below the
-              // bf16 rounding of h).  For g < -88, exp(-g) = inf and the
-              // reciprocal gives 0, the limit of sigmoid.
-              const float h0 = g0 * __fdividef(1.0f, 1.0f + __expf(-g0)) * u0;
-              const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
-              packed[ch * 16 + i] = pack_bf16x2(h0, h1);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tbase + ch * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              packed[ch * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+            // silu(g) = g * sigmoid(g) on the SFU (a few float32 ulps, far
+            // below the bf16 rounding of h; g < -88 gives the limit 0)
+            const float h0 = g0 * __fdividef(1.0f, 1.0f + __expf(-g0)) * u0;
+            const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
+            packed[ch * 16 + i] = pack_bf16x2(h0, h1);
           }
         }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + ch * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[ch * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        }
       }
-      // the accumulator is in registers: release TMEM to the next tile's MMAs
+      // accumulator in registers: release it to the next tile's MMAs
       tc_fence_before();
-      mbar_arrive(&tempty[g]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
       ++tcount;
-      if (!mine) continue;
-      const int row0 = (c.b0 + g) * BM;
-      constexpr int NBOX = kUp ? 2 : 4;  // 64-column output boxes
+      if (rank == 1 && !c.two) continue;  // duplicate rows: nothing to store
+      const int row0 = (c.b0 + static_cast<int>(rank)) * BM;
+      constexpr int NBOX = kUp ? 2 : 4;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
-        if (et == 0) tma_store_wait_read<0>();  // the box's previous store has read `buf`
-        named_barrier_sync(sync_id, EPI_THREADS);
-        // 128-byte swizzle: logical 16-B chunk cidx of row r sits at cidx ^ (r % 8)
+        uint8_t* buf = sEpi + (nstore & 1u) * EPI_BOX_BYTES;
+        if (et == 0) tma_store_wait_read<1>();  // the store that last read `buf` is done
+        named_barrier_sync(1, 128);
         uint8_t* row_ptr = buf + r * 128;
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -396,12 +381,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4*>(row_ptr + ((m ^ (r & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
         }
         fence_proxy_async_smem();
-        named_barrier_sync(sync_id, EPI_THREADS);
+        named_barrier_sync(1, 128);
         if (et == 0) {
           const int col0 = (kUp ? c.j * 128 : c.j * BN) + bx * 64;
-          if (col0 < N_out) tma_store_2d(&tmD, buf, col0, row0);  // no store wholly past the last column
+          if (col0 < N_out) tma_store_2d(&tmD, buf, col0, row0);
           tma_store_commit();
         }
+        ++nstore;
       }
     }
     if (et == 0) tma_store_wait_all<0>();
@@ -409,10 +395,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // neither CTA frees TMEM or exits while the pair still uses it
+  tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -454,7 +441,8 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, const int32_t*
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               P_SMEM_ALLOC);
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
@@ -465,11 +453,25 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, const int32_t*
   const int K = kUp ? s.H : s.I;
   const int64_t mb = max_blocks_of(s);
   const int64_t max_tiles = (mb / 2 + s.E) * NT;  // sum_e ceil(nb_e / 2) <= nb / 2 + E
-  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
-  if (grid <= 0) return cudaSuccess;
-  return launch_pdl(grouped_gemm_kernel<kUp>, dim3(grid), dim3(NUM_THREADS), SMEM_ALLOC, st, maps.a, maps.b0,
-                    maps.b1, maps.d, off_pad, num_blocks, static_cast<int>(mb), s.E, K, NT, kUp ? s.I : s.H,
-                    status);
+  int64_t clusters = num_sms / 2;
+  if (max_tiles < clusters) clusters = max_tiles;
+  if (clusters <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(P_THREADS);
+  cfg.dynamicSmemBytes = P_SMEM_ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kUp>, maps.a, maps.b0, maps.b1, maps.d, off_pad,
+                            num_blocks, static_cast<int>(mb), s.E, K, NT, kUp ? s.I : s.H, status);
 }
 
 }  // namespace

@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
-constexpr int kMaxEPerLane = kMaxE / 32;
 constexpr int kTopkThreads = 32 * kChunkTokens;              // one warp per token of the chunk
 
 // exp(v - m) for float32 v <= m: the difference is split exactly into
