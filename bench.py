@@ -232,12 +232,11 @@ def run_ours(args, world, rank, local):
                            v.block_expert, v.num_blocks, v.gather_idx, v.scatter_idx, ws.data_ptr(), sh)
         if ev is not None:
             ev[1].record(stream)
-        rc |= lib.moe_grouped_gemm_up(sp, x.data_ptr(), v.gather_idx, v.off_pad, v.block_expert,
+        rc |= lib.moe_grouped_gemm_up(sp, x.data_ptr(), v.gather_idx, v.counts, v.off_pad,
                                       v.num_blocks, wg.data_ptr(), wu.data_ptr(), v.h, ws.data_ptr(), sh)
         if ev is not None:
             ev[2].record(stream)
-        rc |= lib.moe_grouped_gemm_down(sp, v.h, v.off_pad, v.block_expert, v.num_blocks, wd.data_ptr(),
-                                        v.Y, ws.data_ptr(), sh)
+        rc |= lib.moe_grouped_gemm_down(sp, v.h, v.counts, v.off_pad, wd.data_ptr(), v.Y, ws.data_ptr(), sh)
         if ev is not None:
             ev[3].record(stream)
         rc |= lib.moe_combine(sp, v.Y, v.scatter_idx, v.topk_w, out.data_ptr(), ws.data_ptr(), sh)

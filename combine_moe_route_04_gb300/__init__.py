@@ -84,7 +84,7 @@ def load():
     lib.moe_grouped_gemm_up.restype = st
     lib.moe_grouped_gemm_up.argtypes = [S] + [P] * 10
     lib.moe_grouped_gemm_down.restype = st
-    lib.moe_grouped_gemm_down.argtypes = [S] + [P] * 8
+    lib.moe_grouped_gemm_down.argtypes = [S] + [P] * 7
     lib.moe_combine.restype = st
     lib.moe_combine.argtypes = [S] + [P] * 6
     lib.moe_forward.restype = st
@@ -235,7 +235,7 @@ def moe_route_noalloc(s, logits, topk_ids, topk_w, counts, off_pad, block_expert
     _check(load().moe_route_noalloc(ctypes.byref(s), *args, _stream(stream)), "moe_route_noalloc")
 
 
-def moe_grouped_gemm_up(s, X, gather_idx, off_pad, block_expert, num_blocks, W_gate, W_up, h, ws,
+def moe_grouped_gemm_up(s, X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, ws,
                         stream=None):
     import torch
     s = _shape_obj(s)
@@ -243,8 +243,8 @@ def moe_grouped_gemm_up(s, X, gather_idx, off_pad, block_expert, num_blocks, W_g
     bf = torch.bfloat16
     args = [_dev_tensor(X, bf, s.T * s.H, "X"),
             _dev_tensor(gather_idx, torch.int32, mr, "gather_idx"),
+            _dev_tensor(counts, torch.int32, s.E, "counts"),
             _dev_tensor(off_pad, torch.int32, s.E + 1, "off_pad"),
-            _dev_tensor(block_expert, torch.int32, mb, "block_expert"),
             _dev_tensor(num_blocks, torch.int32, 1, "num_blocks"),
             _dev_tensor(W_gate, bf, s.E * s.H * s.I, "W_gate"),
             _dev_tensor(W_up, bf, s.E * s.H * s.I, "W_up"),
@@ -253,15 +253,14 @@ def moe_grouped_gemm_up(s, X, gather_idx, off_pad, block_expert, num_blocks, W_g
     _check(load().moe_grouped_gemm_up(ctypes.byref(s), *args, _stream(stream)), "moe_grouped_gemm_up")
 
 
-def moe_grouped_gemm_down(s, h, off_pad, block_expert, num_blocks, W_down, Y, ws, stream=None):
+def moe_grouped_gemm_down(s, h, counts, off_pad, W_down, Y, ws, stream=None):
     import torch
     s = _shape_obj(s)
     mb, mr = capacity(s)
     bf = torch.bfloat16
     args = [_dev_tensor(h, bf, mr * s.I, "h"),
+            _dev_tensor(counts, torch.int32, s.E, "counts"),
             _dev_tensor(off_pad, torch.int32, s.E + 1, "off_pad"),
-            _dev_tensor(block_expert, torch.int32, mb, "block_expert"),
-            _dev_tensor(num_blocks, torch.int32, 1, "num_blocks"),
             _dev_tensor(W_down, bf, s.E * s.I * s.H, "W_down"),
             _dev_tensor(Y, bf, mr * s.H, "Y"),
             _dev_tensor(ws, torch.uint8, workspace_size(s), "ws")]

@@ -107,8 +107,8 @@ Views views_of(const moe_shape& s, void* ws) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx, const int32_t* off_pad,
-                  const int32_t* block_expert, const int32_t* num_blocks, const uint16_t* Wg, const uint16_t* Wu,
+moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx, const int32_t* counts,
+                  const int32_t* off_pad, const int32_t* num_blocks, const uint16_t* Wg, const uint16_t* Wu,
                   uint16_t* h, const Views& w, int num_sms, cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   cudaError_t e = launch_permute_rows(s, X, gather_idx, num_blocks, w.xp, w.status, st);
@@ -118,12 +118,11 @@ moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_i
   if (!encode_bf16_2d(&m.a, w.xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
       !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
     return MOE_ERR_CUDA;
-  return cuda_status(launch_gemm_up(s, m, off_pad, block_expert, num_blocks, w.status, num_sms, st));
+  return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, num_sms, st));
 }
 
-moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* off_pad, const int32_t* block_expert,
-                    const int32_t* num_blocks, const uint16_t* Wd, uint16_t* Y, const Views& w, int num_sms,
-                    cudaStream_t st) {
+moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts, const int32_t* off_pad,
+                    const uint16_t* Wd, uint16_t* Y, const Views& w, int num_sms, cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EI = static_cast<uint64_t>(s.E) * s.I;
@@ -131,7 +130,7 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* off_pa
       !encode_bf16_2d(&m.d, Y, mr, s.H, 128, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
-  return cuda_status(launch_gemm_down(s, m, off_pad, block_expert, num_blocks, w.status, num_sms, st));
+  return cuda_status(launch_gemm_down(s, m, Y, off_pad, counts, w.status, num_sms, st));
 }
 
 }  // namespace
@@ -279,12 +278,12 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
 }
 
 moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const int32_t* gather_idx,
-                               const int32_t* off_pad, const int32_t* block_expert, const int32_t* num_blocks,
+                               const int32_t* counts, const int32_t* off_pad, const int32_t* num_blocks,
                                const moe_bf16* W_gate, const moe_bf16* W_up, moe_bf16* h, void* ws,
                                moe_stream_t stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const void* ptrs[] = {X, gather_idx, off_pad, block_expert, num_blocks, W_gate, W_up, h, ws};
+  const void* ptrs[] = {X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, ws};
   for (const void* p : ptrs) {
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(p)) return MOE_ERR_MISALIGNED;
@@ -293,16 +292,15 @@ moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const 
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_up(*shape, X, gather_idx, off_pad, block_expert, num_blocks, W_gate, W_up, h, views_of(*shape, ws),
-                sms, s);
+  return run_up(*shape, X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, views_of(*shape, ws), sms, s);
 }
 
-moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, const int32_t* off_pad,
-                                 const int32_t* block_expert, const int32_t* num_blocks, const moe_bf16* W_down,
-                                 moe_bf16* Y, void* ws, moe_stream_t stream) {
+moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, const int32_t* counts,
+                                 const int32_t* off_pad, const moe_bf16* W_down, moe_bf16* Y, void* ws,
+                                 moe_stream_t stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const void* ptrs[] = {h, off_pad, block_expert, num_blocks, W_down, Y, ws};
+  const void* ptrs[] = {h, counts, off_pad, W_down, Y, ws};
   for (const void* p : ptrs) {
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(p)) return MOE_ERR_MISALIGNED;
@@ -311,7 +309,7 @@ moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, cons
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_down(*shape, h, off_pad, block_expert, num_blocks, W_down, Y, views_of(*shape, ws), sms, s);
+  return run_down(*shape, h, counts, off_pad, W_down, Y, views_of(*shape, ws), sms, s);
 }
 
 moe_status moe_combine(const moe_shape* shape, const moe_bf16* Y, const int32_t* scatter_idx, const float* topk_w,
@@ -350,9 +348,9 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   if (launch_route(sh, logits, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
                    v.gather_idx, v.scatter_idx, w.chunk_counts, w.status, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = run_up(sh, X, v.gather_idx, v.off_pad, v.block_expert, v.num_blocks, W_gate, W_up, v.h, w, sms, s);
+  st = run_up(sh, X, v.gather_idx, v.counts, v.off_pad, v.num_blocks, W_gate, W_up, v.h, w, sms, s);
   if (st != MOE_OK) return st;
-  st = run_down(sh, v.h, v.off_pad, v.block_expert, v.num_blocks, W_down, v.Y, w, sms, s);
+  st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, sms, s);
   if (st != MOE_OK) return st;
   return cuda_status(launch_combine(sh, v.Y, v.scatter_idx, v.topk_w, out, w.status, s));
 }

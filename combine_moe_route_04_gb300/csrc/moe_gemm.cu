@@ -403,6 +403,352 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Token-window variant ("swap" orientation).  The weights are the M=256 MMA
+// operand (CTA r holds 128 weight columns, N-major boxes read as an MN-major
+// A operand) and the expert's tokens are the N operand: a tile is one window
+// of up to 256 consecutive rows of one expert times 256 weight columns, and
+// N = the window's real row count rounded up to 16, so an expert wastes fewer
+// than 16 rows per window instead of the rest of a 128-row block.  In
+// cta_group::2 the N operand is split between the CTAs: CTA r supplies tokens
+// [r N/2, (r+1) N/2) of the window, and both CTAs' TMEM hold all N token
+// columns for their own 128 weight columns (TMEM lane = weight column).
+//   up:   two MMAs per K step, W_gate columns into accumulator g and the same
+//         W_up columns into accumulator u, so a thread owns g and u of one
+//         column for every token; h = SiLU(g) * u.  512 TMEM columns = g | u,
+//         one accumulator set (the epilogue drain is short against K = H).
+//   down: one MMA per K step; two 256-column accumulators double-buffer the
+//         epilogue.
+// The epilogue writes each column's values down a 128-row box in shared
+// memory (a transpose on the way out) and TMA-stores it.
+constexpr int S_TOK = 256;                               // max tokens per window
+constexpr int S_TOK_BOX = 128;                           // token rows per TMA box (per CTA)
+constexpr int S_W_BYTES = 2 * B_BOX_BYTES;               // 8 KB: 32 k-rows x 128 weight columns
+constexpr int S_T_BYTES = S_TOK_BOX * BK * 2;            // 8 KB: 128 token rows x 32 k (64-byte swizzle)
+constexpr int S_THREADS = 192;
+constexpr int S_GROUP_WINDOWS = 4;                       // L2 grouping of windows inside an expert
+
+template <bool kUp>
+struct SwapCfg {
+  static constexpr int STAGE_BYTES = (kUp ? 2 : 1) * S_W_BYTES + S_T_BYTES;  // up 24 KB, down 16 KB
+  static constexpr int STAGES = kUp ? 9 : 13;
+  static constexpr int NBUF = kUp ? 1 : 2;               // accumulator sets in TMEM
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1;
+  static constexpr int WIN_OFF = BAR_OFF + NUM_BARS * 8 + 16;
+  static constexpr int BYTES = WIN_OFF + (MAX_E + 1) * 4;
+  static constexpr int ALLOC = BYTES + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget (window kernel)");
+};
+
+struct WinCoord {
+  int e;      // expert
+  int j;      // 256-column weight tile
+  int row0;   // first permuted row of the window
+  int rows;   // real rows in the window (1..256)
+  bool ok;
+};
+
+// An expert's c rows are cut into nw = ceil(c / 256) windows of equal size S
+// = round16(ceil(c / nw)) (the last may be shorter), so the windows that
+// share a weight tile take the same time and read it from L2 together.
+// Tile t: expert e (windows w_off[e] .. w_off[e+1]), then groups of
+// S_GROUP_WINDOWS windows, then weight tile, then the window in the group.
+__device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const int32_t* s_win_off,
+                                                  const int32_t* __restrict__ off_pad,
+                                                  const int32_t* __restrict__ counts, int64_t max_rows) {
+  WinCoord c{0, 0, 0, 0, false};
+  const int q = tile / NT;
+  int lo = 0, hi = E;  // last e with s_win_off[e] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_win_off[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  if (e >= E) return c;
+  const int nw = s_win_off[e + 1] - s_win_off[e];
+  const int local = tile - NT * s_win_off[e];
+  if (nw <= 0 || local < 0 || local >= NT * nw) return c;
+  const int g = local / (NT * S_GROUP_WINDOWS);
+  const int rem = local - g * NT * S_GROUP_WINDOWS;
+  const int gs = min(S_GROUP_WINDOWS, nw - g * S_GROUP_WINDOWS);
+  const int w = g * S_GROUP_WINDOWS + rem % gs;
+  const int cnt = __ldg(counts + e);
+  const int S = ((cnt + nw - 1) / nw + 15) / 16 * 16;
+  c.e = e;
+  c.j = rem / gs;
+  c.row0 = __ldg(off_pad + e) + S * w;
+  c.rows = min(S, cnt - S * w);
+  // the window's rows lie inside the expert's padded range
+  const int pad_end = __ldg(off_pad + e + 1);
+  c.ok = c.rows > 0 && c.rows <= S_TOK && c.row0 >= 0 && c.row0 + c.rows <= pad_end && pad_end <= max_rows &&
+         c.j < NT;
+  return c;
+}
+
+template <bool kUp>
+__global__ void __launch_bounds__(S_THREADS, 1)
+    grouped_gemm_window_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmW0,
+                               const __grid_constant__ CUtensorMap tmW1, uint16_t* __restrict__ D,
+                               const int32_t* __restrict__ off_pad, const int32_t* __restrict__ counts, int E,
+                               int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status) {
+  using C = SwapCfg<kUp>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sStage = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = bars + 2 * C::STAGES + C::NBUF;
+  uint64_t* drain = bars + 2 * C::STAGES + 2 * C::NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_win_off = reinterpret_cast<int32_t*>(smem + C::WIN_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::NBUF; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * 4);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    prefetch_tmap(&tmT);
+    prefetch_tmap(&tmW0);
+    prefetch_tmap(&tmW1);
+  }
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+
+  pdl_wait();
+  if (warp == 2) {
+    // windows per expert (ceil(count / 256)) -> exclusive scan, E <= 256
+    constexpr int per = MAX_E / 32;
+    int loc[per];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      int nw = 0;
+      if (e < E) {
+        const int cnt = __ldg(counts + e);
+        nw = cnt > 0 ? (cnt + S_TOK - 1) / S_TOK : 0;
+      }
+      loc[i] = nw;
+      sum += nw;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e <= E) s_win_off[e] = run;
+      run += loc[i];
+    }
+    if (lane == 31 && 32 * per == E) s_win_off[E] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = NT * s_win_off[E];
+  const int KB = K / BK;
+  const int cluster_id = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const uint32_t full0 = map_to_cta(full, 0);
+  const uint32_t tempty0 = map_to_cta(tempty, 0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer (both CTAs)
+    if (elect_one_sync()) {
+      const uint64_t pol_t = policy_evict_last();
+      const uint64_t pol_w = policy_evict_normal();
+      uint32_t it = 0;
+      bool stop = false;
+      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
+        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+        if (!c.ok) {
+          record_status(status, kStatusBounds);
+          continue;
+        }
+        const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
+        const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
+        const int n0 = c.j * 256 + 128 * static_cast<int>(rank);       // its first weight column
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+          uint8_t* st = sStage + s * C::STAGE_BYTES;
+          const uint32_t fb = full0 + 8u * s;
+          const int k0 = c.e * K + kb * BK;
+          tma_load_2d_pair(st, &tmW0, fb, n0, k0, pol_w);
+          tma_load_2d_pair(st + B_BOX_BYTES, &tmW0, fb, n0 + 64, k0, pol_w);
+          if (kUp) {
+            tma_load_2d_pair(st + S_W_BYTES, &tmW1, fb, n0, k0, pol_w);
+            tma_load_2d_pair(st + S_W_BYTES + B_BOX_BYTES, &tmW1, fb, n0 + 64, k0, pol_w);
+          }
+          tma_load_2d_pair(st + (kUp ? 2 : 1) * S_W_BYTES, &tmT, fb, kb * BK, trow, pol_t);
+        }
+      }
+      const uint32_t nst = it < C::STAGES ? it : C::STAGES;
+      for (uint32_t s = 0; s < nst; ++s) {
+        const uint32_t last = s + C::STAGES * ((it - 1 - s) / C::STAGES);
+        int no_abort = 0;
+        mbar_wait(&empty[s], (last / C::STAGES) & 1u, &no_abort, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer (CTA 0)
+    if (rank == 0 && elect_one_sync()) {
+      // M=256 (weights, MN-major A), N from the window, A MN-major, B K-major
+      constexpr uint32_t idesc_base = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((256u >> 4) << 24);
+      uint32_t it = 0;
+      uint32_t tcount = 0;
+      bool stop = false;
+      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
+        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+        if (!c.ok) continue;
+        const uint32_t N = static_cast<uint32_t>(((c.rows + 15) / 16) * 16);
+        const uint32_t idesc = idesc_base | ((N >> 3) << 17);
+        const uint32_t a = C::NBUF == 2 ? (tcount & 1u) : 0u;
+        const uint32_t aph = C::NBUF == 2 ? ((tcount >> 1) & 1u) : (tcount & 1u);
+        if (!mbar_wait(&tempty[a], aph ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(sStage + s * C::STAGE_BYTES);
+          const uint32_t tk = st + (kUp ? 2 : 1) * S_W_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A (weights, this CTA's 128 columns): MN-major, 128-byte swizzle,
+            // 64-column boxes 4 KB apart, 8-row K groups 1 KB apart, K step 2 KB.
+            // B (tokens, this CTA's N/2 rows): K-major, 64-byte swizzle, 8-row
+            // groups 512 B apart, K step 32 B.
+            const uint64_t bdesc = smem_desc(tk + kk * 32, 16, 512, kSwizzle64B);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            tc_mma_f16_pair(d, smem_desc(st + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B), bdesc, idesc, acc);
+            if (kUp)
+              tc_mma_f16_pair(d + 256, smem_desc(st + S_W_BYTES + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B),
+                              bdesc, idesc, acc);
+          }
+          tc_commit_pair(&empty[s], 0x3);
+        }
+        if (stop) break;
+        tc_commit_pair(&tfull[a], 0x3);
+        ++tcount;
+      }
+      tc_commit_pair(drain, 0x1);
+      int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort, status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue (both CTAs)
+    // thread = TMEM lane = weight column `col` of this CTA's 128: it holds
+    // that column for every token of the window and writes it down the
+    // output rows; a warp writes 64 contiguous bytes of one row per store
+    const int q = warp & 3;
+    const int col = q * 32 + lane;
+    uint32_t tcount = 0;
+    for (int tile = cluster_id; tile < total_tiles; tile += nclusters) {
+      const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+      if (!c.ok) continue;
+      const uint32_t a = C::NBUF == 2 ? (tcount & 1u) : 0u;
+      const uint32_t aph = C::NBUF == 2 ? ((tcount >> 1) & 1u) : (tcount & 1u);
+      const bool ok = mbar_wait(&tfull[a], aph, abort_flag, status);
+      if (vote_any_epi(!ok)) break;
+      tc_fence_after();
+      const int nchunks = (c.rows + 31) / 32;       // 32-token TMEM column chunks holding real rows
+      uint32_t packed[S_TOK / 2];                   // bf16 pairs (token 2i, 2i+1) of this column
+      const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+      for (int ch = 0; ch < S_TOK / 32; ++ch) {
+        if (ch < nchunks) {
+          if (kUp) {
+            uint32_t gv[32], uv[32];
+            tmem_ld_32x32b_x32(tbase + ch * 32, gv);
+            tmem_ld_32x32b_x32(tbase + 256 + ch * 32, uv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+              const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+              // silu(g) = g * sigmoid(g) on the SFU (a few float32 ulps, far
+              // below the bf16 rounding of h; g < -88 gives the limit 0)
+              const float h0 = g0 * __fdividef(1.0f, 1.0f + __expf(-g0)) * u0;
+              const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
+              packed[ch * 16 + i] = pack_bf16x2(h0, h1);
+            }
+          } else {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + ch * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[ch * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
+      ++tcount;
+      // out[row0 + t][j*256 + 128 rank + col] for the window's real rows
+      const int colg = c.j * 256 + 128 * static_cast<int>(rank) + col;
+      if (colg < N_out) {
+        uint16_t* dst = D + static_cast<int64_t>(c.row0) * N_out + colg;
+#pragma unroll
+        for (int i = 0; i < S_TOK / 2; ++i) {
+          if (2 * i < c.rows) {
+            const uint32_t v = packed[i];
+            dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
+            if (2 * i + 1 < c.rows) dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ gather_idx,
                                     const int32_t* __restrict__ num_blocks_ptr, int64_t max_rows, int T, int H,
                                     uint16_t* __restrict__ Xp, uint32_t* __restrict__ status) {
@@ -432,34 +778,34 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ X, const int32_
 }
 
 template <bool kUp>
-cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
-                        const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status, int num_sms,
-                        cudaStream_t st) {
-  (void)block_expert;  // tiles are decoded from off_pad
+cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, const int32_t* off_pad,
+                        const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
+  using C = SwapCfg<kUp>;
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               P_SMEM_ALLOC);
+    err = cudaFuncSetAttribute(grouped_gemm_window_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::ALLOC);
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
-  // up: 128 gate + 128 up columns per tile (I % 128 == 0); down: 256 output
-  // columns per tile, the last tile of an H % 256 == 128 row is half outside
-  // the tensor (TMA zero-fills those weight columns and skips the store).
-  const int NT = kUp ? s.I / 128 : (s.H + BN - 1) / BN;
+  // 256 weight columns per tile (up: I % 256 == 0 keeps gate/up slices whole;
+  // down: the last tile of an H % 256 == 128 output is half outside, TMA
+  // zero-fills those weight columns and the store is skipped)
+  const int NT = kUp ? (s.I + 255) / 256 : (s.H + 255) / 256;
   const int K = kUp ? s.H : s.I;
-  const int64_t mb = max_blocks_of(s);
-  const int64_t max_tiles = (mb / 2 + s.E) * NT;  // sum_e ceil(nb_e / 2) <= nb / 2 + E
+  const int64_t T_k = static_cast<int64_t>(s.T) * s.k;
+  const int64_t max_windows = T_k / S_TOK + (s.E < T_k ? s.E : T_k);  // sum_e ceil(c_e / 256)
+  const int64_t max_tiles = max_windows * NT;
   int64_t clusters = num_sms / 2;
   if (max_tiles < clusters) clusters = max_tiles;
   if (clusters <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  cfg.blockDim = dim3(P_THREADS);
-  cfg.dynamicSmemBytes = P_SMEM_ALLOC;
+  cfg.blockDim = dim3(S_THREADS);
+  cfg.dynamicSmemBytes = C::ALLOC;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -470,8 +816,8 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, const int32_t*
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kUp>, maps.a, maps.b0, maps.b1, maps.d, off_pad,
-                            num_blocks, static_cast<int>(mb), s.E, K, NT, kUp ? s.I : s.H, status);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_window_kernel<kUp>, maps.a, maps.b0, maps.b1, D, off_pad, counts,
+                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status);
 }
 
 }  // namespace
@@ -486,16 +832,14 @@ cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int
                     num_blocks, mr, s.T, s.H, Xp, status);
 }
 
-cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
-                           const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status, int num_sms,
-                           cudaStream_t st) {
-  return launch_gemm<true>(s, maps, off_pad, block_expert, num_blocks, status, num_sms, st);
+cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
+                           const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
+  return launch_gemm<true>(s, maps, h, off_pad, counts, status, num_sms, st);
 }
 
-cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
-                             const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status, int num_sms,
-                             cudaStream_t st) {
-  return launch_gemm<false>(s, maps, off_pad, block_expert, num_blocks, status, num_sms, st);
+cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
+                             const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
+  return launch_gemm<false>(s, maps, Y, off_pad, counts, status, num_sms, st);
 }
 
 }  // namespace moe

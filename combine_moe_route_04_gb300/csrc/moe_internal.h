@@ -74,18 +74,16 @@ cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int
                                 const int32_t* num_blocks, uint16_t* Xp, uint32_t* status, cudaStream_t st);
 
 struct GemmMaps {
-  CUtensorMap a;     // A operand rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32
-  CUtensorMap b0;    // up: W_gate [E*H][I]; down: W_down [E*I][H]; box 32 x 64
-  CUtensorMap b1;    // up: W_up   [E*H][I]; down: unused (copy of b0)
+  CUtensorMap a;     // token rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32
+  CUtensorMap b0;    // weights, up: W_gate [E*H][I]; down: W_down [E*I][H]; box 32 x 64
+  CUtensorMap b1;    // weights, up: W_up   [E*H][I]; down: unused (copy of b0)
   CUtensorMap d;     // output rows: h [max_rows][I] or Y [max_rows][H]; box 128 x 64
 };
 
-cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
-                           const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status,
-                           int num_sms, cudaStream_t st);
-cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, const int32_t* off_pad,
-                             const int32_t* block_expert, const int32_t* num_blocks, uint32_t* status,
-                             int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
+                           const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
+                             const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
                            const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);

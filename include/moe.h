@@ -144,27 +144,30 @@ moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
                              moe_stream_t stream);
 
 /* Step 3: grouped gate/up GEMM with the SiLU(gate)*up epilogue.
- *   X      [T, H] bf16 tokens; rows are gathered through gather_idx
+ *   X          [T, H] bf16 tokens; rows are gathered through gather_idx
+ *   gather_idx, counts, off_pad, num_blocks: moe_route's outputs
  *   W_gate [E, H, I] bf16,  W_up [E, H, I] bf16
- *   h      [max_rows, I] bf16 out: h[r] = bf16(silu(g) * u) for every row r
- *          of the first num_blocks blocks; padding rows hold values of no
- *          meaning (never read by the combine)
- *   ws     workspace (scratch: the gathered activation rows)
+ *   h          [max_rows, I] bf16 out: h[r] = bf16(silu(g) * u) for every real
+ *              row r (gather_idx[r] >= 0); padding rows hold values of no
+ *              meaning (never read by the combine)
+ *   ws         workspace (scratch: the gathered activation rows)
  * g and u accumulate in float32 on the tensor cores; SiLU*up is formed in
  * float32 and rounded once to bf16. */
 moe_status moe_grouped_gemm_up(const moe_shape *shape, const moe_bf16 *X,
-                               const int32_t *gather_idx, const int32_t *off_pad,
-                               const int32_t *block_expert, const int32_t *num_blocks,
+                               const int32_t *gather_idx, const int32_t *counts,
+                               const int32_t *off_pad, const int32_t *num_blocks,
                                const moe_bf16 *W_gate, const moe_bf16 *W_up,
                                moe_bf16 *h, void *ws, moe_stream_t stream);
 
 /* Step 4: grouped down GEMM.
- *   h      [max_rows, I] bf16 (permuted rows), W_down [E, I, H] bf16
- *   Y      [max_rows, H] bf16 out: Y[r] = bf16(h[r] W_down[expert of r]) */
+ *   h      [max_rows, I] bf16 (permuted rows), counts / off_pad from moe_route,
+ *   W_down [E, I, H] bf16
+ *   Y      [max_rows, H] bf16 out: Y[r] = bf16(h[r] W_down[expert of r]) for
+ *          every real row r; padding rows hold values of no meaning */
 moe_status moe_grouped_gemm_down(const moe_shape *shape, const moe_bf16 *h,
-                                 const int32_t *off_pad, const int32_t *block_expert,
-                                 const int32_t *num_blocks, const moe_bf16 *W_down,
-                                 moe_bf16 *Y, void *ws, moe_stream_t stream);
+                                 const int32_t *counts, const int32_t *off_pad,
+                                 const moe_bf16 *W_down, moe_bf16 *Y, void *ws,
+                                 moe_stream_t stream);
 
 /* Step 5: top-k weighted combine back to token order, without atomics.
  *   out[t, c] = bf16(sum_{j<k} topk_w[t,j] * Y[scatter_idx[t,j], c])

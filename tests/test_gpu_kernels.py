@@ -42,7 +42,7 @@ def upload_route(moe, s, r):
     be[:r.num_blocks] = r.block_expert
     g = np.full(mr, -1, np.int32)
     g[:r.num_blocks * 128] = r.gather_idx
-    return {"off_pad": to_dev(r.off_pad), "block_expert": to_dev(be),
+    return {"off_pad": to_dev(r.off_pad), "block_expert": to_dev(be), "counts": to_dev(r.counts),
             "num_blocks": to_dev(np.array([r.num_blocks], np.int32)), "gather_idx": to_dev(g),
             "scatter_idx": to_dev(r.scatter_idx), "topk_w": to_dev(r.topk_w)}
 
@@ -62,7 +62,7 @@ def test_grouped_gemms_and_combine(oracle_mod, name):
 
     # up GEMM on the oracle's route
     h = torch.empty((mr, I), dtype=torch.bfloat16, device="cuda")
-    moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["off_pad"], d["block_expert"],
+    moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["counts"], d["off_pad"],
                             d["num_blocks"], to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
     assert moe.last_device_status(ws) == 0
     h_got = host_u16(h)[:r.num_blocks * 128]
@@ -72,8 +72,7 @@ def test_grouped_gemms_and_combine(oracle_mod, name):
     h_ref_dev = torch.zeros((mr, I), dtype=torch.bfloat16, device="cuda")
     h_ref_dev[:r.num_blocks * 128] = to_dev_bf16(ref.h)
     Y = torch.empty((mr, H), dtype=torch.bfloat16, device="cuda")
-    moe.moe_grouped_gemm_down(s, h_ref_dev, d["off_pad"], d["block_expert"], d["num_blocks"],
-                              to_dev_bf16(wd), Y, ws)
+    moe.moe_grouped_gemm_down(s, h_ref_dev, d["counts"], d["off_pad"], to_dev_bf16(wd), Y, ws)
     assert moe.last_device_status(ws) == 0
     y_got = host_u16(Y)[:r.num_blocks * 128]
     assert_rows_close(y_got[real], ref.Y[real], "Y")
@@ -99,7 +98,7 @@ def test_gemm_up_bitwise_deterministic(oracle_mod):
     outs = []
     for _ in range(2):
         h = torch.zeros((mr, I), dtype=torch.bfloat16, device="cuda")
-        moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["off_pad"], d["block_expert"],
+        moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["counts"], d["off_pad"],
                                 d["num_blocks"], to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
         outs.append(host_u16(h)[:r.num_blocks * 128][r.gather_idx >= 0])
     assert np.array_equal(outs[0], outs[1])
