@@ -12,26 +12,30 @@
 //   down: Y[b, j] = bf16(h_b Wd[e][:, j]) for 256-column slices j.
 //
 // Design (the roles and barrier lifetimes of "TIRx 与高性能GEMM (下)" Step 7,
-// and the two-CTA MMA of its Step 8, re-keyed to expert blocks):
-//   * a tile is a PAIR of 128-row blocks of the same expert times one
-//     256-column MMA tile, computed by a cluster of two CTAs on two SMs with
-//     M=256 tcgen05.mma (cta_group::2): CTA r owns block b0 + r (its A rows,
-//     its 128 accumulator rows in its own TMEM) and half of the B tile;
-//   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its A (128x32,
-//     64-byte swizzle) and its B half (32x128 as two 32x64 boxes, N-major,
-//     128-byte swizzle) into a 12-stage SMEM ring; all loads complete on CTA
-//     0's full barriers;
-//   * warp 1 allocates 512 TMEM columns in both CTAs (two 128x256 f32
-//     accumulators each); in CTA 0 one elected lane issues the MMAs and
-//     commits stages back to both producers and finished accumulators to
-//     both epilogues;
-//   * warps 2-5 of each CTA drain the accumulator (thread = row) into
-//     registers (SiLU*up or bf16 cast), release it on CTA 0's
-//     accumulator-empty barrier so the next tile's MMAs overlap this
-//     writeback, and store the rows through a swizzled SMEM box and TMA;
-//   * tile order: expert by expert; inside an expert, groups of GROUP_PAIRS
-//     pairs, all column tiles of a group before the next group, so the
-//     group's A rows stay in L2 while every B tile of the expert streams by.
+// and the two-CTA MMA of its Step 8, re-keyed to expert row windows):
+//   * a cluster of two CTAs on two SMs computes one tile = 256 weight
+//     columns x one window of an expert's rows with M=256 tcgen05.mma
+//     (cta_group::2).  The weights are the M operand: CTA r holds 128 weight
+//     columns (N-major boxes read as an MN-major A operand); the window's
+//     tokens are the N operand (N = real rows rounded up to 16, at most 256),
+//     CTA r supplying tokens [r N/2, (r+1) N/2).  Each CTA's TMEM holds its
+//     128 weight columns (lanes) for all N tokens (columns);
+//   * an expert's rows are cut into equal windows so the tiles sharing a
+//     weight tile run in step and read it from L2 together; padding beyond
+//     the real rows costs at most 15 rows per window;
+//   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its weight
+//     columns (two 32x64 boxes, 128-byte swizzle; the up GEMM loads W_gate
+//     and W_up) and its token rows (128x32, 64-byte swizzle) into a ring of
+//     9 (up) / 13 (down) stages; all loads complete on CTA 0's full barriers;
+//   * warp 1 allocates 512 TMEM columns in both CTAs; in CTA 0 one elected
+//     lane issues the MMAs (the up GEMM issues a W_gate and a W_up MMA per K
+//     step into accumulators g | u, so SiLU(g)*u meets in one thread) and
+//     commits stages back to both producers and results to both epilogues;
+//   * warps 2-5 of each CTA drain the accumulator (thread = weight column)
+//     into registers, release it on CTA 0's accumulator-empty barrier, and
+//     write their column down the window's output rows (a warp stores 64
+//     contiguous bytes of one row).  The down GEMM double-buffers its
+//     256-column accumulators; the up GEMM's g | u fill TMEM.
 // Every wait on an mbarrier is bounded; on a timeout the kernel records it in
 // the status word, the roles stop, in-flight copies and MMAs are drained
 // (bounded) and TMEM is freed before exit.
@@ -45,82 +49,13 @@ namespace {
 
 constexpr int BM = 128;                          // rows per block
 constexpr int BK = 32;                           // K per pipeline stage
-constexpr int BN = 256;                          // MMA N
-constexpr int GROUP_PAIRS = 4;                   // L2 grouping of pairs inside an expert
-constexpr int A_BLOCK_BYTES = BM * BK * 2;       // 8 KB: 128 rows x 64 B (64-byte swizzle)
 constexpr int B_BOX_BYTES = BK * 64 * 2;         // 4 KB: 32 k-rows x 64 columns (128-byte swizzle)
-constexpr int EPI_BOX_BYTES = BM * 64 * 2;       // 16 KB: 128 rows x 64 columns bf16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = 256;
 
 constexpr int MAX_E = 256;
 
-struct TileCoord {
-  int b0;     // first block of the pair
-  int j;      // column tile
-  int e;      // expert
-  bool two;   // second block b0 + 1 present
-  bool ok;
-};
-
-// Tile t of the order: expert e (pairs p_off[e] .. p_off[e+1]), then groups
-// of GROUP_PAIRS pairs, then column tile, then the pair inside the group.
-__device__ __forceinline__ TileCoord decode_tile(int tile, int NT, int E, int num_blocks,
-                                                 const int32_t* s_pair_off, const int32_t* __restrict__ off_pad) {
-  TileCoord c{0, 0, 0, false, false};
-  const int q = tile / NT;  // pair_off[e] <= q < pair_off[e+1]
-  int lo = 0, hi = E;       // last e with s_pair_off[e] <= q
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pair_off[mid] <= q) lo = mid; else hi = mid - 1;
-  }
-  const int e = lo;
-  if (e >= E) return c;
-  const int np = s_pair_off[e + 1] - s_pair_off[e];
-  const int local = tile - NT * s_pair_off[e];
-  if (np <= 0 || local < 0 || local >= NT * np) return c;
-  const int g = local / (NT * GROUP_PAIRS);
-  const int rem = local - g * NT * GROUP_PAIRS;
-  const int gs = min(GROUP_PAIRS, np - g * GROUP_PAIRS);
-  const int p = g * GROUP_PAIRS + rem % gs;
-  const int blk0 = __ldg(off_pad + e) / BM;
-  const int nbe = (__ldg(off_pad + e + 1) - __ldg(off_pad + e)) / BM;
-  c.j = rem / gs;
-  c.b0 = blk0 + 2 * p;
-  c.two = 2 * p + 1 < nbe;
-  c.e = e;
-  c.ok = c.b0 + (c.two ? 1 : 0) < num_blocks && c.j < NT;
-  return c;
-}
-
-// ---------------------------------------------------------------------------
-// CTA-pair variant: a cluster of two CTAs on two SMs computes one 256-row x
-// 256-column tile with M=256 MMAs (cta_group::2): CTA r holds block b0 + r of
-// the pair (128 rows of A, 128 rows of the accumulator in its own TMEM) and
-// HALF of the 256-column B tile (up: CTA 0 the gate columns, CTA 1 the up
-// columns; down: the lower / upper 128 columns).  Per SM, each stage moves
-// 8 KB of A and 8 KB of B and the tensor core reads its half of B once for
-// both SMs, which halves the shared-memory traffic per MMA of the single-CTA
-// kernel; the accumulator is 256 TMEM columns per CTA, so two accumulators
-// double-buffer the epilogue against the next tile's MMAs.  CTA 0 issues the
-// MMAs; both CTAs' loads complete on CTA 0's full barriers; its commits
-// arrive on both CTAs' empty / accumulator-full barriers; both CTAs' epilogue
-// warps release the accumulator on CTA 0's accumulator-empty barrier.  When
-// the pair has only one block, CTA 1 loads block b0's rows again and stores
-// nothing.
-constexpr int P_STAGES = 12;
-constexpr int P_B_HALF_BYTES = 2 * B_BOX_BYTES;                 // 8 KB: 32 k-rows x 128 columns
-constexpr int P_STAGE_BYTES = A_BLOCK_BYTES + P_B_HALF_BYTES;   // 16 KB
-constexpr int P_THREADS = 192;                                  // producer, MMA, 4 epilogue warps
-constexpr int P_SMEM_EPI_OFF = P_STAGES * P_STAGE_BYTES;
-constexpr int P_SMEM_BAR_OFF = P_SMEM_EPI_OFF + 2 * EPI_BOX_BYTES;
-constexpr int P_NUM_BARS = 2 * P_STAGES + 2 + 2 + 1;           // full, empty, tmem_full[2], tmem_empty[2], drain
-constexpr int P_SMEM_PAIR_OFF = P_SMEM_BAR_OFF + P_NUM_BARS * 8 + 16;
-constexpr int P_SMEM_BYTES = P_SMEM_PAIR_OFF + (MAX_E + 1) * 4;
-constexpr int P_SMEM_ALLOC = P_SMEM_BYTES + 1024;
-static_assert(P_SMEM_ALLOC <= 232448, "shared memory budget (pair kernel)");
-constexpr uint32_t kIdescPair = idesc_bf16_f32(256, 256, /*b_mn_major=*/true);
-
+// OR-vote over the 128 epilogue threads (named barrier 2).
 __device__ __forceinline__ bool vote_any_epi(bool flag) {
   uint32_t r;
   asm volatile(
@@ -132,275 +67,6 @@ __device__ __forceinline__ bool vote_any_epi(bool flag) {
       : "r"(flag ? 1u : 0u)
       : "memory");
   return r != 0;
-}
-
-template <bool kUp>
-__global__ void __launch_bounds__(P_THREADS, 1)
-    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmD,
-                             const int32_t* __restrict__ off_pad, const int32_t* __restrict__ num_blocks_ptr,
-                             int max_blocks, int E, int K, int NT, int N_out, uint32_t* __restrict__ status) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sStage = smem;
-  uint8_t* sEpi = smem + P_SMEM_EPI_OFF;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_SMEM_BAR_OFF);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + P_STAGES;
-  uint64_t* tfull = bars + 2 * P_STAGES;
-  uint64_t* tempty = bars + 2 * P_STAGES + 2;
-  uint64_t* drain = bars + 2 * P_STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_pair_off = reinterpret_cast<int32_t*>(smem + P_SMEM_PAIR_OFF);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
-  pdl_launch_dependents();
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < P_STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * 4);  // one arrival per epilogue warp of both CTAs
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbarrier_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB0);
-    prefetch_tmap(&tmB1);
-    prefetch_tmap(&tmD);
-  }
-  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
-  if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, TMEM_COLS);
-    tmem_relinquish_pair();
-  }
-
-  pdl_wait();
-  int num_blocks = __ldg(num_blocks_ptr);
-  if (num_blocks > max_blocks || num_blocks < 0) {
-    if (threadIdx.x == 0) record_status(status, kStatusBounds);
-    num_blocks = num_blocks < 0 ? 0 : max_blocks;
-  }
-  if (warp == 2) {
-    constexpr int per = MAX_E / 32;
-    int loc[per];
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      int np = 0;
-      if (e < E) {
-        const int nb = (__ldg(off_pad + e + 1) - __ldg(off_pad + e)) / BM;
-        np = nb > 0 ? (nb + 1) / 2 : 0;
-      }
-      loc[i] = np;
-      sum += np;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e <= E) s_pair_off[e] = run;
-      run += loc[i];
-    }
-    if (lane == 31 && 32 * per == E) s_pair_off[E] = incl;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = NT * s_pair_off[E];
-  const int KB = K / BK;
-  const int cluster_id = blockIdx.x >> 1;
-  const int nclusters = gridDim.x >> 1;
-  const uint32_t full0 = map_to_cta(full, 0);      // CTA 0's full barriers (shared::cluster)
-  const uint32_t tempty0 = map_to_cta(tempty, 0);  // CTA 0's accumulator-empty barriers
-
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer (both CTAs)
-    if (elect_one_sync()) {
-      const uint64_t pol_a = policy_evict_last();
-      const uint64_t pol_b = policy_evict_normal();
-      const CUtensorMap* mapB = (kUp && rank == 1) ? &tmB1 : &tmB0;
-      uint32_t it = 0;
-      bool stop = false;
-      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
-        const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
-        if (!c.ok) {
-          record_status(status, kStatusBounds);
-          continue;
-        }
-        const int my_b = c.b0 + ((rank == 1 && c.two) ? 1 : 0);
-        const int n0 = kUp ? c.j * 128 : c.j * BN + 128 * static_cast<int>(rank);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const uint32_t s = it % P_STAGES;
-          const uint32_t ph = (it / P_STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
-            stop = true;
-            break;
-          }
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P_STAGE_BYTES);
-          uint8_t* st = sStage + s * P_STAGE_BYTES;
-          const uint32_t fb = full0 + 8u * s;
-          const int k0 = c.e * K + kb * BK;
-          tma_load_2d_pair(st, &tmA, fb, kb * BK, my_b * BM, pol_a);
-          tma_load_2d_pair(st + A_BLOCK_BYTES, mapB, fb, n0, k0, pol_b);
-          tma_load_2d_pair(st + A_BLOCK_BYTES + B_BOX_BYTES, mapB, fb, n0 + 64, k0, pol_b);
-        }
-      }
-      // drain: every issued stage was consumed by the MMAs (so its copies landed)
-      const uint32_t nst = it < P_STAGES ? it : P_STAGES;
-      for (uint32_t s = 0; s < nst; ++s) {
-        const uint32_t last = s + P_STAGES * ((it - 1 - s) / P_STAGES);
-        int no_abort = 0;
-        mbar_wait(&empty[s], (last / P_STAGES) & 1u, &no_abort, status);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer (CTA 0)
-    if (rank == 0 && elect_one_sync()) {
-      uint32_t it = 0;
-      uint32_t tcount = 0;
-      bool stop = false;
-      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
-        const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
-        if (!c.ok) continue;
-        const uint32_t a = tcount & 1u;
-        const uint32_t aph = (tcount >> 1) & 1u;
-        if (!mbar_wait(&tempty[a], aph ^ 1u, abort_flag, status)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + a * ACC_COLS;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const uint32_t s = it % P_STAGES;
-          const uint32_t ph = (it / P_STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, status)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = smem_u32(sStage + s * P_STAGE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // A (each CTA's 128 rows): K-major, 64-byte swizzle, 8-row groups
-            // 512 B apart, 16-wide K step = 32 B.  B (each CTA's 128
-            // columns): N-major, 128-byte swizzle, 64-column boxes 4 KB apart,
-            // 8-row K groups 1 KB apart, 16-wide K step = 2 KB.
-            tc_mma_f16_pair(d, smem_desc(st + kk * 32, 16, 512, kSwizzle64B),
-                            smem_desc(st + A_BLOCK_BYTES + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B), kIdescPair,
-                            (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit_pair(&empty[s], 0x3);
-        }
-        if (stop) break;
-        tc_commit_pair(&tfull[a], 0x3);
-        ++tcount;
-      }
-      tc_commit_pair(drain, 0x1);
-      int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort, status);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------ epilogue (both CTAs)
-    const int et = threadIdx.x - 64;
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    uint32_t tcount = 0;
-    uint32_t nstore = 0;
-    constexpr int NPACK = kUp ? 64 : 128;
-    for (int tile = cluster_id; tile < total_tiles; tile += nclusters) {
-      const TileCoord c = decode_tile(tile, NT, E, num_blocks, s_pair_off, off_pad);
-      if (!c.ok) continue;
-      const uint32_t a = tcount & 1u;
-      const uint32_t aph = (tcount >> 1) & 1u;
-      const bool ok = mbar_wait(&tfull[a], aph, abort_flag, status);
-      if (vote_any_epi(!ok)) break;
-      tc_fence_after();
-      uint32_t packed[NPACK];
-      const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-      if (kUp) {
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t gv[32], uv[32];
-          tmem_ld_32x32b_x32(tbase + ch * 32, gv);
-          tmem_ld_32x32b_x32(tbase + 128 + ch * 32, uv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-            // silu(g) = g * sigmoid(g) on the SFU (a few float32 ulps, far
-            // below the bf16 rounding of h; g < -88 gives the limit 0)
-            const float h0 = g0 * __fdividef(1.0f, 1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
-            packed[ch * 16 + i] = pack_bf16x2(h0, h1);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + ch * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[ch * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        }
-      }
-      // accumulator in registers: release it to the next tile's MMAs
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
-      ++tcount;
-      if (rank == 1 && !c.two) continue;  // duplicate rows: nothing to store
-      const int row0 = (c.b0 + static_cast<int>(rank)) * BM;
-      constexpr int NBOX = kUp ? 2 : 4;
-#pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) {
-        uint8_t* buf = sEpi + (nstore & 1u) * EPI_BOX_BYTES;
-        if (et == 0) tma_store_wait_read<1>();  // the store that last read `buf` is done
-        named_barrier_sync(1, 128);
-        uint8_t* row_ptr = buf + r * 128;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const uint32_t* src = packed + bx * 32 + 4 * m;
-          *reinterpret_cast<uint4*>(row_ptr + ((m ^ (r & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
-        }
-        fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (et == 0) {
-          const int col0 = (kUp ? c.j * 128 : c.j * BN) + bx * 64;
-          if (col0 < N_out) tma_store_2d(&tmD, buf, col0, row0);
-          tma_store_commit();
-        }
-        ++nstore;
-      }
-    }
-    if (et == 0) tma_store_wait_all<0>();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();  // neither CTA frees TMEM or exits while the pair still uses it
-  tc_fence_after();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc_pair(tmem_base, TMEM_COLS);
-  }
 }
 
 // ---------------------------------------------------------------------------
