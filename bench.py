@@ -163,7 +163,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import moe_inputs
-    cfg = moe_inputs.config(WORKLOAD)
+    cfg = moe_inputs.config(args.workload)
     inp = moe_inputs.make_inputs(cfg)
     per_step_s = max(2.0, 20.0 / max(1, args.steps + args.warmup))
     vals = []
@@ -186,6 +186,7 @@ def run_reference(args, world, rank):
 
 
 def run_ours(args, world, rank, local):
+    workload = args.workload
     import numpy as np
     import torch
 
@@ -203,7 +204,7 @@ def run_ours(args, world, rank, local):
         torch.distributed.barrier()
     moe.load()
 
-    cfg = moe_inputs.config(WORKLOAD)
+    cfg = moe_inputs.config(workload)
     inp = moe_inputs.make_inputs(cfg)
     T, H, I, E, k = cfg.shape
     s = moe.shape(T, H, I, E, k)
@@ -300,28 +301,54 @@ def run_ours(args, world, rank, local):
     fwd_ms = f0.elapsed_time(f1) / K
 
     # ---------------- end to end: host buffers, copies inside the timed region
+    # Every step copies its inputs (logits, X) from pinned host memory and its
+    # output back.  The copies run on a second stream, double-buffered, so
+    # step i+1's inputs and step i-1's output move while step i computes.
     logits_h = torch.from_numpy(inp["logits"]).pin_memory()
     x_h = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    logits_d = torch.empty_like(logits)
-    x_d = torch.empty_like(x)
+    out_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    logits_d = [torch.empty_like(logits) for _ in range(2)]
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    out_d = [torch.empty_like(out) for _ in range(2)]
+    cs_in = torch.cuda.Stream(device=dev)    # host -> device copies
+    cs_out = torch.cuda.Stream(device=dev)   # device -> host copies (the link is full duplex)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot b copied in
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # forward of slot b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # output of slot b copied out
     Ke = max(10, K // 4)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(Ke):
-            logits_d.copy_(logits_h, non_blocking=True)
-            x_d.copy_(x_h, non_blocking=True)
-            moe.moe_forward_raw(s, logits_d.data_ptr(), x_d.data_ptr(), wg.data_ptr(), wu.data_ptr(),
-                                wd.data_ptr(), out.data_ptr(), ws.data_ptr(), sh)
-            out_h.copy_(out, non_blocking=True)
-        e1.record(stream)
+    e0.record(cs_in)
+    cs_out.wait_event(e0)
+    stream.wait_event(e0)
+    for i in range(Ke):
+        b = i & 1
+        with torch.cuda.stream(cs_in):
+            if i >= 2:
+                cs_in.wait_event(ev_done[b])    # step i-2 no longer reads these inputs
+            logits_d[b].copy_(logits_h, non_blocking=True)
+            x_d[b].copy_(x_h, non_blocking=True)
+            ev_in[b].record(cs_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])        # step i-2's output has been copied out
+        moe.moe_forward_raw(s, logits_d[b].data_ptr(), x_d[b].data_ptr(), wg.data_ptr(), wu.data_ptr(),
+                            wd.data_ptr(), out_d[b].data_ptr(), ws.data_ptr(), sh)
+        ev_done[b].record(stream)
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(ev_done[b])
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            ev_out[b].record(cs_out)
+    cs_in.wait_event(ev_out[(Ke - 1) & 1])
+    cs_in.wait_event(ev_out[Ke & 1])
+    e1.record(cs_in)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / Ke
+    if not torch.equal(out_h[(Ke - 1) & 1], out_d[(Ke - 1) & 1].cpu()):
+        raise RuntimeError("end-to-end output copy mismatch")
     h2d = logits_h.numel() * 4 + x_h.numel() * 2
-    d2h = out_h.numel() * 2
+    d2h = out_h[0].numel() * 2
 
     # ---------------- aggregate over ranks (max time)
     ms_step = total_ms / K
@@ -340,7 +367,7 @@ def run_ours(args, world, rank, local):
     up_flops = 4.0 * T * k * H * I
     achieved = up_flops / (up_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops_sustained"]
-    traffic = recorded_traffic("grouped_gemm_up")
+    traffic = recorded_traffic("grouped_gemm_up") if workload == WORKLOAD else None
     cpu_v, cpu_desc, cpu_cores, _ = cpu_oracle_sample(cfg, inp, seconds=12.0)
     counts = ws[v.counts - ws.data_ptr():v.counts - ws.data_ptr() + 4 * E].view(torch.int32).cpu().numpy()
     touched = int((counts > 0).sum())
@@ -419,7 +446,7 @@ def main():
                     help="run --warmup forwards, then one more forward, and exit (no timing): "
                          "the command line for ncu captures")
     ap.add_argument("--workload", type=int, default=WORKLOAD,
-                    help="with --profile: which workload (1-5) to run")
+                    help="which workload (1-5) to time (default: the pages-shaped layer)")
     ap.add_argument("--shape", type=str, default=None,
                     help="with --profile: T,H,I,E,k of a synthetic shape instead of a workload")
     args = ap.parse_args()
