@@ -383,7 +383,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "per_kernel_us": {n: statistics.mean(vv) * 1e3 for n, vv in parts.items()},
         "forward_call_us": fwd_ms * 1e3,
-        "roofline": {"kernel": "moe_grouped_gemm_up call (row gather + CTA-pair tcgen05 grouped GEMM)",
+        "roofline": {"kernel": "moe_grouped_gemm_up call (row gather + token-window CTA-pair tcgen05 grouped GEMM)",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": "%s bf16_tflops_sustained" % pk_src,
