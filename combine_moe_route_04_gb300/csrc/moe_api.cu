@@ -118,7 +118,7 @@ moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_i
   if (!encode_bf16_2d(&m.a, w.xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
       !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
     return MOE_ERR_CUDA;
-  return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, num_sms, st));
+  return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), num_sms, st));
 }
 
 moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts, const int32_t* off_pad,
@@ -130,7 +130,7 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts
       !encode_bf16_2d(&m.d, Y, mr, s.H, 128, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
-  return cuda_status(launch_gemm_down(s, m, Y, off_pad, counts, w.status, num_sms, st));
+  return cuda_status(launch_gemm_down(s, m, Y, off_pad, counts, w.status, ws_sched_down(w.status), num_sms, st));
 }
 
 }  // namespace

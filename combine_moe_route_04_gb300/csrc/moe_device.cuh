@@ -65,16 +65,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for a barrier that the other CTA
+// of the pair arrives on (its writes before the arrival become visible).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase of `bar` with the given parity has completed.  Gives
 // up when *abort becomes non-zero (another role gave up) or after
 // kWaitLimitNs; on a timeout it records kStatusTimeout and raises *abort.
-// Returns false when it gave up.
+// Returns false when it gave up.  kClusterScope: acquire at cluster scope.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((i & 15u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {

@@ -93,6 +93,10 @@ constexpr int S_W_BYTES = 2 * B_BOX_BYTES;               // 8 KB: 32 k-rows x 12
 constexpr int S_T_BYTES = S_TOK_BOX * BK * 2;            // 8 KB: 128 token rows x 32 k (64-byte swizzle)
 constexpr int S_THREADS = 192;
 constexpr int S_GROUP_WINDOWS = 4;                       // L2 grouping of windows inside an expert
+constexpr int S_TILE_RING = 8;                           // tile indices in flight from the scheduler
+// readers of each tile index: CTA 0's MMA lane and 4 epilogue warps, CTA 1's
+// producer lane and 4 epilogue warps (CTA 0's producer lane is the scheduler)
+constexpr int S_TILE_READERS = 1 + 4 + 1 + 4;
 
 template <bool kUp>
 struct SwapCfg {
@@ -100,9 +104,10 @@ struct SwapCfg {
   static constexpr int STAGES = kUp ? 9 : 13;
   static constexpr int NBUF = kUp ? 1 : 2;               // accumulator sets in TMEM
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1 + 2 * S_TILE_RING;
   static constexpr int WIN_OFF = BAR_OFF + NUM_BARS * 8 + 16;
-  static constexpr int BYTES = WIN_OFF + (MAX_E + 1) * 4;
+  static constexpr int TILE_OFF = (WIN_OFF + (MAX_E + 1) * 4 + 15) / 16 * 16;
+  static constexpr int BYTES = TILE_OFF + S_TILE_RING * 4;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget (window kernel)");
 };
@@ -152,13 +157,77 @@ __device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const
   return c;
 }
 
+// Dynamic tile scheduler.  CTA 0's producer lane draws tile indices from a
+// counter in global memory (atomicAdd, in tile order, so the windows that
+// share a weight tile are still drawn together) and publishes each into a
+// ring in both CTAs' shared memory; every other role of the pair reads the
+// same sequence from its own CTA's ring.  A cluster draws and publishes its
+// next tile when it starts the current one, so the index is in place a whole
+// tile before any role needs it, and clusters that got smaller windows take
+// more tiles.  The cluster that finishes drawing last resets the counter for
+// the next launch.
+struct TileRing {
+  uint64_t* full;        // [S_TILE_RING], this CTA: one arrival (the scheduler)
+  uint64_t* empty;       // [S_TILE_RING], used in CTA 0: S_TILE_READERS arrivals
+  volatile int32_t* idx; // [S_TILE_RING], this CTA
+};
+
+// Reader side: the index of the n-th tile of this cluster; -1 when a bounded
+// wait gave up.  CTA 0's readers synchronise at CTA scope, CTA 1's at cluster
+// scope.  With release == false the caller releases the slot (ring_release).
+__device__ __forceinline__ void ring_release(const TileRing& r, uint32_t n, uint32_t rank, uint32_t empty0_cluster) {
+  const uint32_t slot = n % S_TILE_RING;
+  if (rank == 0) mbar_arrive(&r.empty[slot]);
+  else mbar_arrive_cluster(empty0_cluster + 8u * slot);
+}
+__device__ __forceinline__ int ring_take(const TileRing& r, uint32_t n, uint32_t rank, uint32_t empty0_cluster,
+                                         bool release, volatile int* abort, uint32_t* status) {
+  const uint32_t slot = n % S_TILE_RING;
+  const uint32_t ph = (n / S_TILE_RING) & 1u;
+  const bool ok = rank == 0 ? mbar_wait<false>(&r.full[slot], ph, abort, status)
+                            : mbar_wait<true>(&r.full[slot], ph, abort, status);
+  if (!ok) return -1;
+  const int t = r.idx[slot];
+  if (release) ring_release(r, n, rank, empty0_cluster);
+  return t;
+}
+
+// Scheduler side (CTA 0): publish the n-th tile index to both CTAs.
+__device__ __forceinline__ bool ring_put(const TileRing& r, uint32_t n, int tile, volatile int* abort,
+                                         uint32_t* status) {
+  const uint32_t slot = n % S_TILE_RING;
+  if (!mbar_wait(&r.empty[slot], ((n / S_TILE_RING) & 1u) ^ 1u, abort, status)) return false;
+  r.idx[slot] = tile;
+  mbar_arrive(&r.full[slot]);
+  const uint32_t remote_idx = map_to_cta(const_cast<int32_t*>(&r.idx[slot]), 1);
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_idx), "r"(tile) : "memory");
+  mbar_arrive_cluster(map_to_cta(&r.full[slot], 1));
+  return true;
+}
+
+// Draws the next tile index; a value past every possible draw means the
+// counter was not cleared (moe_workspace_init) and ends the sequence.
+__device__ __forceinline__ int draw_tile(uint32_t* ctr, int total_tiles, int nclusters, uint32_t* status) {
+  const uint32_t t = atomicAdd(ctr, 1u);
+  if (t >= static_cast<uint32_t>(total_tiles + nclusters)) {
+    record_status(status, kStatusBounds);
+    return total_tiles;
+  }
+  return static_cast<int>(t);
+}
+
 template <bool kUp>
 __global__ void __launch_bounds__(S_THREADS, 1)
     grouped_gemm_window_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmW0,
                                const __grid_constant__ CUtensorMap tmW1, uint16_t* __restrict__ D,
                                const int32_t* __restrict__ off_pad, const int32_t* __restrict__ counts, int E,
-                               int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status) {
+                               int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status,
+                               uint32_t* __restrict__ sched) {
   using C = SwapCfg<kUp>;
+  // the up GEMM draws its tiles dynamically (its windows differ in size and
+  // there are few tiles per cluster); the down GEMM, with many short tiles,
+  // keeps the static round-robin order
+  constexpr bool kDyn = kUp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStage = smem;
@@ -168,6 +237,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   uint64_t* tfull = bars + 2 * C::STAGES;
   uint64_t* tempty = bars + 2 * C::STAGES + C::NBUF;
   uint64_t* drain = bars + 2 * C::STAGES + 2 * C::NBUF;
+  const TileRing ring{bars + 2 * C::STAGES + 2 * C::NBUF + 1, bars + 2 * C::STAGES + 2 * C::NBUF + 1 + S_TILE_RING,
+                      reinterpret_cast<volatile int32_t*>(smem + C::TILE_OFF)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_win_off = reinterpret_cast<int32_t*>(smem + C::WIN_OFF);
@@ -187,6 +258,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       mbar_init(&tempty[a], 2 * 4);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < S_TILE_RING; ++i) {
+      mbar_init(&ring.full[i], 1);
+      mbar_init(&ring.empty[i], S_TILE_READERS);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tmap(&tmT);
@@ -237,10 +312,11 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = NT * s_win_off[E];
   const int KB = K / BK;
-  const int cluster_id = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
+  const int cluster_id = blockIdx.x >> 1;
   const uint32_t full0 = map_to_cta(full, 0);
   const uint32_t tempty0 = map_to_cta(tempty, 0);
+  const uint32_t rempty0 = map_to_cta(ring.empty, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer (both CTAs)
@@ -249,16 +325,38 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       const uint64_t pol_w = policy_evict_normal();
       uint32_t it = 0;
       bool stop = false;
-      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
-        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
-        if (!c.ok) {
-          record_status(status, kStatusBounds);
-          continue;
+      // CTA 0 draws the pair's tiles and publishes them; CTA 1 reads them
+      int tile = cluster_id;
+      if (kDyn) {
+        if (rank == 0) {
+          tile = draw_tile(sched, total_tiles, nclusters, status);
+          stop = !ring_put(ring, 0, tile, abort_flag, status);
+        } else {
+          tile = ring_take(ring, 0, rank, rempty0, true, abort_flag, status);
         }
+      }
+      for (uint32_t n = 0; !stop && tile >= 0 && tile < total_tiles; ++n) {
+        // CTA 0 draws the next tile now without waiting for the value, and
+        // publishes it halfway through this tile's loads
+        const uint32_t raw_next = kDyn && rank == 0 ? atomicAdd(sched, 1u) : 0u;
+        int next = tile + nclusters;
+        bool published = !kDyn || rank != 0;
+        auto publish = [&]() {
+          next = raw_next < static_cast<uint32_t>(total_tiles + nclusters) ? static_cast<int>(raw_next) : total_tiles;
+          if (next != static_cast<int>(raw_next)) record_status(status, kStatusBounds);
+          published = true;
+          return ring_put(ring, n + 1, next, abort_flag, status);
+        };
+        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+        if (!c.ok) record_status(status, kStatusBounds);
         const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
         const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
         const int n0 = c.j * 256 + 128 * static_cast<int>(rank);       // its first weight column
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = 0; c.ok && kb < KB; ++kb, ++it) {
+          if (!published && kb == KB / 2 && !publish()) {
+            stop = true;
+            break;
+          }
           const uint32_t s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
@@ -277,6 +375,18 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           }
           tma_load_2d_pair(st + (kUp ? 2 : 1) * S_W_BYTES, &tmT, fb, kb * BK, trow, pol_t);
         }
+        if (stop) break;
+        if (!published && !publish()) break;
+        tile = !kDyn || rank == 0 ? next : ring_take(ring, n + 1, rank, rempty0, true, abort_flag, status);
+      }
+      if (kDyn && rank == 0) {
+        // this cluster has drawn its last index; the last cluster to get here
+        // clears the counter for the next launch
+        __threadfence();
+        if (atomicAdd(sched + 1, 1u) == static_cast<uint32_t>(nclusters - 1)) {
+          atomicExch(sched, 0u);
+          atomicExch(sched + 1, 0u);
+        }
       }
       const uint32_t nst = it < C::STAGES ? it : C::STAGES;
       for (uint32_t s = 0; s < nst; ++s) {
@@ -294,7 +404,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       uint32_t it = 0;
       uint32_t tcount = 0;
       bool stop = false;
-      for (int tile = cluster_id; tile < total_tiles && !stop; tile += nclusters) {
+      for (uint32_t n = 0; !stop; ++n) {
+        const int tile = kDyn ? ring_take(ring, n, rank, rempty0, true, abort_flag, status)
+                              : cluster_id + static_cast<int>(n) * nclusters;
+        if (tile < 0 || tile >= total_tiles) break;
         const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
         if (!c.ok) continue;
         const uint32_t N = static_cast<uint32_t>(((c.rows + 15) / 16) * 16);
@@ -346,7 +459,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     const int q = warp & 3;
     const int col = q * 32 + lane;
     uint32_t tcount = 0;
-    for (int tile = cluster_id; tile < total_tiles; tile += nclusters) {
+    for (uint32_t n = 0;; ++n) {
+      int tile = cluster_id + static_cast<int>(n) * nclusters;
+      if (kDyn) {
+        tile = ring_take(ring, n, rank, rempty0, false, abort_flag, status);
+        __syncwarp();
+        if (lane == 0) ring_release(ring, n, rank, rempty0);
+        if (vote_any_epi(tile < 0)) break;
+      }
+      if (tile >= total_tiles) break;
       const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
       if (!c.ok) continue;
       const uint32_t a = C::NBUF == 2 ? (tcount & 1u) : 0u;
@@ -445,7 +566,7 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ X, const int32_
 
 template <bool kUp>
 cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, const int32_t* off_pad,
-                        const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
+                        const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms, cudaStream_t st) {
   using C = SwapCfg<kUp>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -483,7 +604,7 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_window_kernel<kUp>, maps.a, maps.b0, maps.b1, D, off_pad, counts,
-                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status);
+                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status, sched);
 }
 
 }  // namespace
@@ -499,13 +620,15 @@ cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int
 }
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
-                           const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
-  return launch_gemm<true>(s, maps, h, off_pad, counts, status, num_sms, st);
+                           const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
+                           cudaStream_t st) {
+  return launch_gemm<true>(s, maps, h, off_pad, counts, status, sched, num_sms, st);
 }
 
 cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
-                             const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st) {
-  return launch_gemm<false>(s, maps, Y, off_pad, counts, status, num_sms, st);
+                             const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
+                             cudaStream_t st) {
+  return launch_gemm<false>(s, maps, Y, off_pad, counts, status, sched, num_sms, st);
 }
 
 }  // namespace moe

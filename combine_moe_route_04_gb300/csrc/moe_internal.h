@@ -45,6 +45,10 @@ moe_status device_ready(cudaStream_t st, int* num_sms);
 moe_status validate_shape(const moe_shape* s);
 
 inline uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
+// tile-scheduler counters of the two GEMMs, inside the first 256 bytes that
+// moe_workspace_init clears (separate 64-byte lines)
+inline uint32_t* ws_sched_up(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 16; }
+inline uint32_t* ws_sched_down(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 32; }
 
 // Launch with programmatic stream serialisation (the kernel must call
 // pdl_wait() before touching memory its predecessors use).
@@ -80,10 +84,14 @@ struct GemmMaps {
   CUtensorMap d;     // output rows: h [max_rows][I] or Y [max_rows][H]; box 128 x 64
 };
 
+// sched: the kernel's tile counter and its done counter (two uint32 in the
+// workspace's first 256 bytes, zero between launches)
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
-                           const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st);
+                           const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
+                           cudaStream_t st);
 cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
-                             const int32_t* counts, uint32_t* status, int num_sms, cudaStream_t st);
+                             const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
+                             cudaStream_t st);
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
                            const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);

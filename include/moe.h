@@ -87,8 +87,11 @@ moe_status moe_capacity(const moe_shape *shape, int64_t *max_blocks, int64_t *ma
  * of one shape; calls sharing it must be ordered on one stream. */
 moe_status moe_workspace_size(const moe_shape *shape, size_t *bytes);
 
-/* Clears the workspace status word.  Call once after allocating `ws`
- * (asynchronous, on `stream`). */
+/* Clears the workspace status word and the gate/up GEMM's tile counter (all
+ * in the first 256 bytes of `ws`).  Call once after allocating `ws`
+ * (asynchronous, on `stream`); the GEMM leaves its counter cleared for the
+ * next call.  On a workspace that was never cleared the gate/up GEMM may
+ * skip tiles; it reports MOE_ERR_DEVICE_BOUNDS when a draw is out of range. */
 moe_status moe_workspace_init(const moe_shape *shape, void *ws, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the error recorded by the kernels since the
@@ -150,7 +153,8 @@ moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
  *   h          [max_rows, I] bf16 out: h[r] = bf16(silu(g) * u) for every real
  *              row r (gather_idx[r] >= 0); padding rows hold values of no
  *              meaning (never read by the combine)
- *   ws         workspace (scratch: the gathered activation rows)
+ *   ws         workspace (scratch: the gathered activation rows; the tile
+ *              counter the kernel's clusters draw their tiles from)
  * g and u accumulate in float32 on the tensor cores; SiLU*up is formed in
  * float32 and rounded once to bf16. */
 moe_status moe_grouped_gemm_up(const moe_shape *shape, const moe_bf16 *X,
