@@ -233,8 +233,8 @@ def run_ours(args, world, rank, local):
                            v.block_expert, v.num_blocks, v.gather_idx, v.scatter_idx, ws.data_ptr(), sh)
         if ev is not None:
             ev[1].record(stream)
-        rc |= lib.moe_grouped_gemm_up(sp, x.data_ptr(), v.gather_idx, v.counts, v.off_pad,
-                                      v.num_blocks, wg.data_ptr(), wu.data_ptr(), v.h, ws.data_ptr(), sh)
+        rc |= lib.moe_grouped_gemm_up(sp, x.data_ptr(), v.scatter_idx, v.counts, v.off_pad,
+                                      wg.data_ptr(), wu.data_ptr(), v.h, ws.data_ptr(), sh)
         if ev is not None:
             ev[2].record(stream)
         rc |= lib.moe_grouped_gemm_down(sp, v.h, v.counts, v.off_pad, wd.data_ptr(), v.Y, ws.data_ptr(), sh)

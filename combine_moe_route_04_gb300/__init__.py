@@ -82,7 +82,7 @@ def load():
     lib.moe_route_noalloc.restype = st
     lib.moe_route_noalloc.argtypes = [S] + [P] * 10
     lib.moe_grouped_gemm_up.restype = st
-    lib.moe_grouped_gemm_up.argtypes = [S] + [P] * 10
+    lib.moe_grouped_gemm_up.argtypes = [S] + [P] * 9
     lib.moe_grouped_gemm_down.restype = st
     lib.moe_grouped_gemm_down.argtypes = [S] + [P] * 7
     lib.moe_combine.restype = st
@@ -235,17 +235,15 @@ def moe_route_noalloc(s, logits, topk_ids, topk_w, counts, off_pad, block_expert
     _check(load().moe_route_noalloc(ctypes.byref(s), *args, _stream(stream)), "moe_route_noalloc")
 
 
-def moe_grouped_gemm_up(s, X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, ws,
-                        stream=None):
+def moe_grouped_gemm_up(s, X, scatter_idx, counts, off_pad, W_gate, W_up, h, ws, stream=None):
     import torch
     s = _shape_obj(s)
     mb, mr = capacity(s)
     bf = torch.bfloat16
     args = [_dev_tensor(X, bf, s.T * s.H, "X"),
-            _dev_tensor(gather_idx, torch.int32, mr, "gather_idx"),
+            _dev_tensor(scatter_idx, torch.int32, s.T * s.k, "scatter_idx"),
             _dev_tensor(counts, torch.int32, s.E, "counts"),
             _dev_tensor(off_pad, torch.int32, s.E + 1, "off_pad"),
-            _dev_tensor(num_blocks, torch.int32, 1, "num_blocks"),
             _dev_tensor(W_gate, bf, s.E * s.H * s.I, "W_gate"),
             _dev_tensor(W_up, bf, s.E * s.H * s.I, "W_up"),
             _dev_tensor(h, bf, mr * s.I, "h"),

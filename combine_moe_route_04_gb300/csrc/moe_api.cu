@@ -107,11 +107,11 @@ Views views_of(const moe_shape& s, void* ws) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx, const int32_t* counts,
-                  const int32_t* off_pad, const int32_t* num_blocks, const uint16_t* Wg, const uint16_t* Wu,
+moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, const int32_t* counts,
+                  const int32_t* off_pad, const uint16_t* Wg, const uint16_t* Wu,
                   uint16_t* h, const Views& w, int num_sms, cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
-  cudaError_t e = launch_permute_rows(s, X, gather_idx, num_blocks, w.xp, w.status, st);
+  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, w.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
@@ -277,13 +277,12 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
                                   gather_idx, scatter_idx, w.chunk_counts, w.status, s));
 }
 
-moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const int32_t* gather_idx,
-                               const int32_t* counts, const int32_t* off_pad, const int32_t* num_blocks,
-                               const moe_bf16* W_gate, const moe_bf16* W_up, moe_bf16* h, void* ws,
-                               moe_stream_t stream) {
+moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const int32_t* scatter_idx,
+                               const int32_t* counts, const int32_t* off_pad, const moe_bf16* W_gate,
+                               const moe_bf16* W_up, moe_bf16* h, void* ws, moe_stream_t stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const void* ptrs[] = {X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, ws};
+  const void* ptrs[] = {X, scatter_idx, counts, off_pad, W_gate, W_up, h, ws};
   for (const void* p : ptrs) {
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(p)) return MOE_ERR_MISALIGNED;
@@ -292,7 +291,7 @@ moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const 
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_up(*shape, X, gather_idx, counts, off_pad, num_blocks, W_gate, W_up, h, views_of(*shape, ws), sms, s);
+  return run_up(*shape, X, scatter_idx, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), sms, s);
 }
 
 moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, const int32_t* counts,
@@ -348,7 +347,7 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   if (launch_route(sh, logits, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
                    v.gather_idx, v.scatter_idx, w.chunk_counts, w.status, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = run_up(sh, X, v.gather_idx, v.counts, v.off_pad, v.num_blocks, W_gate, W_up, v.h, w, sms, s);
+  st = run_up(sh, X, v.scatter_idx, v.counts, v.off_pad, W_gate, W_up, v.h, w, sms, s);
   if (st != MOE_OK) return st;
   st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, sms, s);
   if (st != MOE_OK) return st;

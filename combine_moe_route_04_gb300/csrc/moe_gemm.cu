@@ -536,31 +536,49 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   }
 }
 
-__global__ void permute_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ gather_idx,
-                                    const int32_t* __restrict__ num_blocks_ptr, int64_t max_rows, int T, int H,
-                                    uint16_t* __restrict__ Xp, uint32_t* __restrict__ status) {
+// Fills Xp (the token rows in permuted order) token by token: a warp takes
+// one token and a 1024-column chunk, reads that piece of X once and writes it
+// to the token's k rows (scatter_idx).  Each row of X is read from memory
+// once, in order, however many experts picked it; padding rows of Xp are left
+// untouched (the GEMM never stores their results).
+__global__ void scatter_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ scatter_idx,
+                                    int64_t max_rows, int T, int H, int k, uint16_t* __restrict__ Xp,
+                                    uint32_t* __restrict__ status) {
   pdl_launch_dependents();
   pdl_wait();
-  int64_t rows = static_cast<int64_t>(__ldg(num_blocks_ptr)) * BM;
-  if (rows > max_rows || rows < 0) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, kStatusBounds);
-    rows = rows < 0 ? 0 : max_rows;
-  }
+  constexpr int CH = 1024;  // columns per work item: 16 bytes x 4 per lane
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int vec_per_row = H / 8;
-  for (int64_t row = warp0; row < rows; row += nwarps) {
-    const int t = __ldg(gather_idx + row);
-    if (t < 0) continue;
-    if (t >= T) {
-      if (lane == 0) record_status(status, kStatusBounds);
-      continue;
+  const int nchunk = (H + CH - 1) / CH;
+  const int64_t items = static_cast<int64_t>(T) * nchunk;
+  for (int64_t item = warp0; item < items; item += nwarps) {
+    const int t = static_cast<int>(item / nchunk);
+    const int c0 = static_cast<int>(item % nchunk) * CH;
+    int my_row = -1;  // lane j < k: row of (t, j)
+    if (lane < k) {
+      const int32_t r = __ldg(scatter_idx + static_cast<int64_t>(t) * k + lane);
+      if (r >= 0 && r < max_rows) my_row = r;
+      else record_status(status, kStatusBounds);
     }
-    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(Xp + row * H);
-#pragma unroll 4
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    const int nv = min(CH, H - c0) / 8;  // 16-byte vectors in this chunk (H % 128 == 0)
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(t) * H + c0);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = lane + 32 * u;
+      if (idx < nv) v[u] = __ldg(src + idx);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (row < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(row) * H + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = lane + 32 * u;
+        if (idx < nv) dst[idx] = v[u];
+      }
+    }
   }
 }
 
@@ -609,14 +627,13 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
 
 }  // namespace
 
-cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx,
-                                const int32_t* num_blocks, uint16_t* Xp, uint32_t* status, cudaStream_t st) {
-  const int64_t mr = max_rows_of(s);
-  const int threads = 256;
-  int64_t blocks = (mr + 7) / 8;
+cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
+                                uint32_t* status, cudaStream_t st) {
+  const int64_t items = static_cast<int64_t>(s.T) * ((s.H + 1023) / 1024);
+  int64_t blocks = (items + 7) / 8;  // 8 warps (items) per CTA
   if (blocks > 4096) blocks = 4096;
-  return launch_pdl(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, X, gather_idx,
-                    num_blocks, mr, s.T, s.H, Xp, status);
+  return launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, X, scatter_idx,
+                    max_rows_of(s), s.T, s.H, s.k, Xp, status);
 }
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,

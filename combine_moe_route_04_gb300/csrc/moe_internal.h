@@ -74,8 +74,9 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
                          int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
                          uint32_t* status, cudaStream_t st);
 
-cudaError_t launch_permute_rows(const moe_shape& s, const uint16_t* X, const int32_t* gather_idx,
-                                const int32_t* num_blocks, uint16_t* Xp, uint32_t* status, cudaStream_t st);
+// Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token.
+cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
+                                uint32_t* status, cudaStream_t st);
 
 struct GemmMaps {
   CUtensorMap a;     // token rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32

@@ -147,8 +147,11 @@ moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
                              moe_stream_t stream);
 
 /* Step 3: grouped gate/up GEMM with the SiLU(gate)*up epilogue.
- *   X          [T, H] bf16 tokens; rows are gathered through gather_idx
- *   gather_idx, counts, off_pad, num_blocks: moe_route's outputs
+ *   X          [T, H] bf16 tokens
+ *   scatter_idx, counts, off_pad: moe_route's outputs; the call first copies
+ *              X[t] to permuted row scatter_idx[t, j] of a workspace buffer
+ *              (token by token, so each row of X is read once), then runs
+ *              the GEMM over each expert's rows
  *   W_gate [E, H, I] bf16,  W_up [E, H, I] bf16
  *   h          [max_rows, I] bf16 out: h[r] = bf16(silu(g) * u) for every real
  *              row r (gather_idx[r] >= 0); padding rows hold values of no
@@ -158,10 +161,10 @@ moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
  * g and u accumulate in float32 on the tensor cores; SiLU*up is formed in
  * float32 and rounded once to bf16. */
 moe_status moe_grouped_gemm_up(const moe_shape *shape, const moe_bf16 *X,
-                               const int32_t *gather_idx, const int32_t *counts,
-                               const int32_t *off_pad, const int32_t *num_blocks,
-                               const moe_bf16 *W_gate, const moe_bf16 *W_up,
-                               moe_bf16 *h, void *ws, moe_stream_t stream);
+                               const int32_t *scatter_idx, const int32_t *counts,
+                               const int32_t *off_pad, const moe_bf16 *W_gate,
+                               const moe_bf16 *W_up, moe_bf16 *h, void *ws,
+                               moe_stream_t stream);
 
 /* Step 4: grouped down GEMM.
  *   h      [max_rows, I] bf16 (permuted rows), counts / off_pad from moe_route,

@@ -62,8 +62,8 @@ def test_grouped_gemms_and_combine(oracle_mod, name):
 
     # up GEMM on the oracle's route
     h = torch.empty((mr, I), dtype=torch.bfloat16, device="cuda")
-    moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["counts"], d["off_pad"],
-                            d["num_blocks"], to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
+    moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["scatter_idx"], d["counts"], d["off_pad"],
+                            to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
     assert moe.last_device_status(ws) == 0
     h_got = host_u16(h)[:r.num_blocks * 128]
     assert_rows_close(h_got[real], ref.h[real], "h")
@@ -98,7 +98,7 @@ def test_gemm_up_bitwise_deterministic(oracle_mod):
     outs = []
     for _ in range(2):
         h = torch.zeros((mr, I), dtype=torch.bfloat16, device="cuda")
-        moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["gather_idx"], d["counts"], d["off_pad"],
-                                d["num_blocks"], to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
+        moe.moe_grouped_gemm_up(s, to_dev_bf16(x), d["scatter_idx"], d["counts"], d["off_pad"],
+                                to_dev_bf16(wg), to_dev_bf16(wu), h, ws)
         outs.append(host_u16(h)[:r.num_blocks * 128][r.gather_idx >= 0])
     assert np.array_equal(outs[0], outs[1])
