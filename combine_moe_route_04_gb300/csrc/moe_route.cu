@@ -14,17 +14,21 @@
 //
 // Kernels:
 //   1. route_topk_hist: one CTA = one chunk of 32 tokens, one warp per token;
-//      top-k by k rounds of a warp max over packed (logit, index) keys; then
-//      warp 0 ranks the chunk's entries with __match_any_sync + popc (stable
-//      in-chunk rank per expert) and writes the chunk's histogram.
+//      each lane sorts its few packed (logit, index) keys, then k rounds of a
+//      warp max over the lanes' leading keys (two 32-bit warp reductions: the
+//      logit word, then the index word among the tied lanes); each
+//      pick sets its token's bit in a per-expert 32-bit mask (shared-memory
+//      OR), so an entry's stable in-chunk rank is the popcount of its
+//      expert's mask below its token and the chunk's count the whole
+//      popcount.
 //   2. route_chunk_scan: one warp per expert scans its chunk histogram (the
 //      chunk bases) and writes the expert's row count.
 //   3. route_scatter: every CTA scans the padded counts (off_pad) in shared
 //      memory; one thread per (t, j) writes row = off_pad[e] + chunk base +
 //      in-chunk rank to scatter_idx and gather_idx; the block table and the
 //      padding rows' -1 are spread over all threads.
-// Integer atomics are not used, so every output is a pure function of the
-// logits.
+// The only atomics are those shared-memory ORs, whose result does not depend
+// on their order, so every output is a pure function of the logits.
 #include <cfloat>
 #include <cstdint>
 #include <mutex>
@@ -36,7 +40,6 @@ namespace moe {
 namespace {
 
 constexpr int kMaxE = 256;
-constexpr int kMaxK = 16;
 constexpr int kTopkThreads = 32 * kChunkTokens;              // one warp per token of the chunk
 
 // exp(v - m) for float32 v <= m: the difference is split exactly into
@@ -68,15 +71,15 @@ __device__ __forceinline__ int key_expert(uint64_t key) { return 0xFFFF - static
 
 // Kernel 1: one CTA per chunk of 32 tokens, one warp per token: the k best
 // experts (k rounds of a warp-wide max over the keys, the winner removed
-// each round; slot j = j-th round) and the renormalised weights; then warp 0
-// forms the chunk's expert histogram and each entry's stable in-chunk rank.
+// each round; slot j = j-th round) and the renormalised weights; then the
+// chunk's expert histogram and each entry's stable in-chunk rank from the
+// per-expert token masks.
 // EPL = logits per lane (E <= 32 * EPL).
 template <int EPL>
 __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
     const float* __restrict__ logits, int T, int E, int k, int nch, int32_t* __restrict__ topk_ids,
     float* __restrict__ topk_w, int32_t* __restrict__ local_rank, int32_t* __restrict__ chunk_counts) {
-  __shared__ int32_t s_ids[kChunkTokens * kMaxK];
-  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ uint32_t s_mask[kMaxE];  // bit w: token w of the chunk picked expert e
 
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
@@ -85,9 +88,11 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   const int t0 = chunk * kChunkTokens;
   const int ntok = min(kChunkTokens, T - t0);
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
+  __syncthreads();
   pdl_wait();  // inputs and outputs may be in use by the previous kernel until here
 
+  int my_e = 0;
   if (warp < ntok) {
     const int t = t0 + warp;
     const float* row = logits + static_cast<int64_t>(t) * E;
@@ -97,23 +102,35 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
       const int e = lane + 32 * i;
       key[i] = (e < E) ? pick_key(__ldg(row + e), e) : 0ull;
     }
+    // this lane's keys in descending order (a small exchange network)
+#pragma unroll
+    for (int a = 0; a < EPL - 1; ++a) {
+#pragma unroll
+      for (int b = EPL - 1; b > a; --b) {
+        const uint64_t x = key[b - 1], y = key[b];
+        key[b - 1] = x > y ? x : y;
+        key[b] = x > y ? y : x;
+      }
+    }
+    // round j: the warp's largest leading key is pick j; its lane pops it
+    // (keys are unique, so exactly one lane holds it)
     uint64_t my_key = 0;
     for (int j = 0; j < k; ++j) {
-      uint64_t best = key[0];
+      const uint32_t hi = static_cast<uint32_t>(key[0] >> 32);
+      const uint32_t lo = static_cast<uint32_t>(key[0]);
+      const uint32_t best_hi = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t best_lo = __reduce_max_sync(0xffffffffu, hi == best_hi ? lo : 0u);
+      const uint64_t best = (static_cast<uint64_t>(best_hi) << 32) | best_lo;
+      if (key[0] == best) {
 #pragma unroll
-      for (int i = 1; i < EPL; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
+        for (int i = 0; i < EPL - 1; ++i) key[i] = key[i + 1];
+        key[EPL - 1] = 0ull;
       }
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) key[i] = (key[i] == best) ? 0ull : key[i];  // keys are unique
       if (lane == j) my_key = best;
     }
     // the first pick is the row maximum
     const float m = key_logit(__shfl_sync(0xffffffffu, my_key, 0));
-    const int my_e = key_expert(my_key);
+    my_e = key_expert(my_key);
     const float my_x = (lane < k) ? exp_diff(key_logit(my_key), m) : 0.0f;
     // w_j = x_j / sum_{j' in slot order} x_j' (the softmax denominator
     // cancels); slots hold non-increasing x, so Fast2Sum keeps the rounding
@@ -129,32 +146,16 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
     if (lane < k) {
       topk_ids[static_cast<int64_t>(t) * k + lane] = my_e;
       topk_w[static_cast<int64_t>(t) * k + lane] = my_x / S;
-      s_ids[warp * k + lane] = my_e;
+      atomicOr(&s_mask[my_e], 1u << warp);  // a token picks an expert at most once
     }
   }
   __syncthreads();
-
-  if (warp == 0) {
-    // stable rank of every (t, j) of the chunk among the chunk's entries of
-    // the same expert, entries in (t, j) order: one batch of 32 entries at a
-    // time, peers with the same expert found by __match_any_sync
-    const int n = ntok * k;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      const bool act = i < n;
-      const int key = act ? s_ids[i] : -1 - lane;
-      const uint32_t peers = __match_any_sync(0xffffffffu, key);
-      int r = 0;
-      if (act) r = s_cnt[key] + __popc(peers & lt_mask);
-      __syncwarp();
-      if (act && (__ffs(peers) - 1) == lane) s_cnt[key] += __popc(peers);
-      __syncwarp();
-      if (act) local_rank[static_cast<int64_t>(t0) * k + i] = r;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[static_cast<int64_t>(e) * nch + chunk] = s_cnt[e];
+  // stable rank of (t, j) among the chunk's entries of its expert, entries in
+  // (t, j) order = the chunk's earlier tokens that picked the same expert
+  if (warp < ntok && lane < k)
+    local_rank[static_cast<int64_t>(t0 + warp) * k + lane] = __popc(s_mask[my_e] & ((1u << warp) - 1u));
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<int64_t>(e) * nch + chunk] = __popc(s_mask[e]);
 }
 
 // Kernel 2: one warp per expert: exclusive scan of its chunk histogram (the
@@ -168,17 +169,26 @@ __global__ void __launch_bounds__(256) route_chunk_scan_kernel(int E, int nch, i
   if (e >= E) return;
   int32_t* cc = chunk_counts + static_cast<int64_t>(e) * nch;
   int running = 0;
-  for (int c0 = 0; c0 < nch; c0 += 32) {
-    const int c = c0 + lane;
-    const int v = (c < nch) ? cc[c] : 0;
-    int incl = v;
+  constexpr int U = 8;  // 32-chunk batches loaded before any is scanned
+  for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+    int v[U];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u + lane;
+      v[u] = (c < nch) ? cc[c] : 0;
     }
-    if (c < nch) cc[c] = running + incl - v;
-    running += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u + lane;
+      int incl = v[u];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (c < nch) cc[c] = running + incl - v[u];
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
   if (lane == 0) counts[e] = running;
 }
