@@ -4,8 +4,11 @@
 A step is one pass of the whole layer (route -> grouped gate/up GEMM with
 SiLU*up -> grouped down GEMM -> combine) over one batch of the pages-shaped
 workload (T=2048 tokens, H=4096, I=1536, E=64 experts, top-8), synthetic
-inputs already resident in HBM.  The metric is useful bf16 TFLOP/s
-(6*T*k*H*I FLOPs per step) with microseconds per layer beside it.
+inputs already resident in HBM, timed as K calls of moe_forward (the
+library's one-call layer) between two CUDA events.  The metric is useful
+bf16 TFLOP/s (6*T*k*H*I FLOPs per step) with microseconds per layer beside
+it; a second pass through the four step calls, with events between them,
+gives the per-step breakdown and the up call's roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -259,9 +262,10 @@ def run_ours(args, world, rank, local):
     if moe.last_device_status(ws, sh) != 0:
         raise RuntimeError("device status after warm-up")
 
-    # ---------------- timed region: K steps, per-step events on the launching stream
+    # ---------------- timed region: K layers, one moe_forward call each (the
+    # seven kernels chained with programmatic dependent launch), events on the
+    # launching stream around all K
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
@@ -272,14 +276,25 @@ def run_ours(args, world, rank, local):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for i in range(K):
-            step_by_step(evs[i])
+        for _ in range(K):
+            forward()
         t_end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if rank == 0 else None
     total_ms = t_start.elapsed_time(t_end)
+    if moe.last_device_status(ws, sh) != 0:
+        raise RuntimeError("device status after timed region")
+
+    # ---------------- breakdown: the same K layers as the four C-ABI steps
+    # with an event between each (the events also cut the launch overlap
+    # between the steps, so these sum to a little more than the layer)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            step_by_step(evs[i])
+    torch.cuda.synchronize(dev)
     parts = {"route": [], "up": [], "down": [], "combine": []}
     for e in evs:
         parts["route"].append(e[0].elapsed_time(e[1]))
@@ -287,18 +302,8 @@ def run_ours(args, world, rank, local):
         parts["down"].append(e[2].elapsed_time(e[3]))
         parts["combine"].append(e[3].elapsed_time(e[4]))
     if moe.last_device_status(ws, sh) != 0:
-        raise RuntimeError("device status after timed region")
-
-    # forward() (one C call per step) over the same K steps, for reference
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        f0.record(stream)
-        for _ in range(K):
-            forward()
-        f1.record(stream)
-    torch.cuda.synchronize(dev)
-    fwd_ms = f0.elapsed_time(f1) / K
+        raise RuntimeError("device status after the breakdown")
+    steps_ms = sum(e[0].elapsed_time(e[4]) for e in evs) / K
 
     # ---------------- end to end: host buffers, copies inside the timed region
     # Every step copies its inputs (logits, X) from pinned host memory and its
@@ -394,7 +399,7 @@ def run_ours(args, world, rank, local):
                          % (3 * E * H * I * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "per_kernel_us": {n: statistics.mean(vv) * 1e3 for n, vv in parts.items()},
-        "forward_call_us": fwd_ms * 1e3,
+        "step_by_step_us": steps_ms * 1e3,
         "roofline": dict(roof, kernel="moe_grouped_gemm_up call (row gather + token-window CTA-pair "
                                       "tcgen05 grouped GEMM)",
                          traffic=traffic, algorithmic_bytes_per_launch=up_bytes,
