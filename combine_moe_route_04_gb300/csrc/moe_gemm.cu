@@ -33,8 +33,9 @@
 //     commits stages back to both producers and results to both epilogues;
 //   * warps 2-5 of each CTA drain the accumulator (thread = weight column)
 //     into registers, release it on CTA 0's accumulator-empty barrier, and
-//     write their column down the window's output rows (a warp stores 64
-//     contiguous bytes of one row).  The down GEMM double-buffers its
+//     write their column down the window's output rows (in the up GEMM
+//     neighbouring lanes swap token halves and store two columns of one
+//     token each).  The down GEMM double-buffers its
 //     256-column accumulators; the up GEMM's g | u fill TMEM.
 // Every wait on an mbarrier is bounded; on a timeout the kernel records it in
 // the status word, the roles stop, in-flight copies and MMAs are drained
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     // ------------------------------------------------------ epilogue (both CTAs)
     // thread = TMEM lane = weight column `col` of this CTA's 128: it holds
     // that column for every token of the window and writes it down the
-    // output rows; a warp writes 64 contiguous bytes of one row per store
+    // output rows
     const int q = warp & 3;
     const int col = q * 32 + lane;
     uint32_t tcount = 0;
@@ -510,9 +511,14 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
       ++tcount;
-      // out[row0 + t][j*256 + 128 rank + col] for the window's real rows
+      // out[row0 + t][j*256 + 128 rank + col] for the window's real rows.
+      // Up GEMM: neighbouring lanes (columns 2m, 2m+1) swap halves of their
+      // token pairs, so the even lane stores token 2i and the odd lane token
+      // 2i+1, each as two adjacent columns (4 bytes): half as many stores.
+      // Down GEMM (short tiles, double-buffered): one column per lane and
+      // 2-byte stores measured faster than paying for the shuffles.
       const int colg = c.j * 256 + 128 * static_cast<int>(rank) + col;
-      if (colg < N_out) {
+      if (!kUp && colg < N_out) {
         uint16_t* dst = D + static_cast<int64_t>(c.row0) * N_out + colg;
 #pragma unroll
         for (int i = 0; i < S_TOK / 2; ++i) {
@@ -520,6 +526,20 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             const uint32_t v = packed[i];
             dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
             if (2 * i + 1 < c.rows) dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+          }
+        }
+      }
+      if (kUp && colg < N_out) {  // uniform across the warp (N_out % 128 == 0)
+        const int odd = lane & 1;
+        uint32_t* dst =
+            reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + odd) * N_out + (colg & ~1));
+#pragma unroll
+        for (int i = 0; i < S_TOK / 2; ++i) {
+          if (2 * i < c.rows) {
+            const uint32_t mine = packed[i];
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            const uint32_t v = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
+            if (2 * i + odd < c.rows) dst[static_cast<int64_t>(i) * N_out] = v;  // two rows = N_out words
           }
         }
       }
