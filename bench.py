@@ -134,6 +134,24 @@ def layer_flops(cfg) -> float:
     return 6.0 * cfg.T * cfg.k * cfg.H * cfg.I
 
 
+def max_over_ranks(values, device=None):
+    """Each value's maximum over the ranks of the default process group (the
+    slowest replica sets the step time); the values unchanged on one rank."""
+    import torch
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_tflops(world: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the layer, so
+    N ranks do N layers' work in the slowest rank's step time."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(cfg, inp, seconds=15.0, max_tokens=256):
     """Times the oracle on the host cores on a bounded sample of the workload:
     routing for all tokens, then tokens' outputs one by one until ~`seconds`.
@@ -356,17 +374,13 @@ def run_ours(args, world, rank, local):
     d2h = out_h[0].numel() * 2
 
     # ---------------- aggregate over ranks (max time)
-    ms_step = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = t.tolist()
+    ms_step, e2e_ms = max_over_ranks([total_ms / K, e2e_ms], dev)
     if rank != 0:
         return 0
 
     flops = layer_flops(cfg)
-    value = world * flops / (ms_step * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, flops, ms_step)
+    e2e_value = aggregate_tflops(world, flops, e2e_ms)
     pk, pk_src = peaks()
     up_ms = statistics.mean(parts["up"])
     up_flops = 4.0 * T * k * H * I
