@@ -31,8 +31,10 @@
 //     lane issues the MMAs (the up GEMM issues a W_gate and a W_up MMA per K
 //     step into accumulators g | u, so SiLU(g)*u meets in one thread) and
 //     commits stages back to both producers and results to both epilogues;
-//   * warps 2-5 of each CTA drain the accumulator (thread = weight column)
-//     into registers, release it on CTA 0's accumulator-empty barrier, and
+//   * warps 2-9 of each CTA drain the accumulator (thread = weight column;
+//     two warps per 32-lane TMEM quarter, each taking half of the window's
+//     tokens) into registers, release it on CTA 0's accumulator-empty
+//     barrier, and
 //     write their column down the window's output rows (in the up GEMM
 //     neighbouring lanes swap token halves and store two columns of one
 //     token each).  The down GEMM double-buffers its
@@ -48,7 +50,6 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                          // rows per block
 constexpr int BK = 32;                           // K per pipeline stage
 constexpr int B_BOX_BYTES = BK * 64 * 2;         // 4 KB: 32 k-rows x 64 columns (128-byte swizzle)
 constexpr uint32_t TMEM_COLS = 512;
@@ -56,16 +57,21 @@ constexpr uint32_t ACC_COLS = 256;
 
 constexpr int MAX_E = 256;
 
-// OR-vote over the 128 epilogue threads (named barrier 2).
+// Epilogue warps: two per 32-lane TMEM quarter (a warp may read only the
+// quarter warp_id % 4), each draining and storing half of the window's tokens.
+constexpr int S_EPI_WARPS = 8;
+constexpr int S_EPI_SPLIT = S_EPI_WARPS / 4;             // warps sharing a lane quarter
+
+// OR-vote over the epilogue threads (named barrier 2).
 __device__ __forceinline__ bool vote_any_epi(bool flag) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, 2, 128, pi;\n\t"
+      "bar.red.or.pred po, 2, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
-      : "r"(flag ? 1u : 0u)
+      : "r"(flag ? 1u : 0u), "n"(S_EPI_WARPS * 32)
       : "memory");
   return r != 0;
 }
@@ -92,12 +98,12 @@ constexpr int S_TOK = 256;                               // max tokens per windo
 constexpr int S_TOK_BOX = 128;                           // token rows per TMA box (per CTA)
 constexpr int S_W_BYTES = 2 * B_BOX_BYTES;               // 8 KB: 32 k-rows x 128 weight columns
 constexpr int S_T_BYTES = S_TOK_BOX * BK * 2;            // 8 KB: 128 token rows x 32 k (64-byte swizzle)
-constexpr int S_THREADS = 192;
+constexpr int S_THREADS = (2 + S_EPI_WARPS) * 32;        // producer, MMA, epilogue warps
 constexpr int S_GROUP_WINDOWS = 4;                       // L2 grouping of windows inside an expert
 constexpr int S_TILE_RING = 8;                           // tile indices in flight from the scheduler
 // readers of each tile index: CTA 0's MMA lane and 4 epilogue warps, CTA 1's
 // producer lane and 4 epilogue warps (CTA 0's producer lane is the scheduler)
-constexpr int S_TILE_READERS = 1 + 4 + 1 + 4;
+constexpr int S_TILE_READERS = 1 + S_EPI_WARPS + 1 + S_EPI_WARPS;
 
 template <bool kUp>
 struct SwapCfg {
@@ -256,7 +262,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     }
     for (int a = 0; a < C::NBUF; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * 4);  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], 2 * S_EPI_WARPS);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     for (int i = 0; i < S_TILE_RING; ++i) {
@@ -457,8 +463,11 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     // thread = TMEM lane = weight column `col` of this CTA's 128: it holds
     // that column for every token of the window and writes it down the
     // output rows
-    const int q = warp & 3;
+    const int q = warp & 3;                                   // TMEM lane quarter
     const int col = q * 32 + lane;
+    constexpr int CH_PER = S_TOK / 32 / S_EPI_SPLIT;          // 32-token chunks per warp
+    const int ch0 = ((warp - 2) / 4) * CH_PER;                // this warp's first chunk
+    const int tok0 = ch0 * 32;                                // ... and first token
     uint32_t tcount = 0;
     for (uint32_t n = 0;; ++n) {
       int tile = cluster_id + static_cast<int>(n) * nclusters;
@@ -477,10 +486,11 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       if (vote_any_epi(!ok)) break;
       tc_fence_after();
       const int nchunks = (c.rows + 31) / 32;       // 32-token TMEM column chunks holding real rows
-      uint32_t packed[S_TOK / 2];                   // bf16 pairs (token 2i, 2i+1) of this column
+      uint32_t packed[CH_PER * 16];                 // bf16 pairs (token tok0+2i, +1) of this column
       const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
-      for (int ch = 0; ch < S_TOK / 32; ++ch) {
+      for (int cl = 0; cl < CH_PER; ++cl) {
+        const int ch = ch0 + cl;
         if (ch < nchunks) {
           if (kUp) {
             uint32_t gv[32], uv[32];
@@ -495,7 +505,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
               // below the bf16 rounding of h; g < -88 gives the limit 0)
               const float h0 = g0 * __fdividef(1.0f, 1.0f + __expf(-g0)) * u0;
               const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
-              packed[ch * 16 + i] = pack_bf16x2(h0, h1);
+              packed[cl * 16 + i] = pack_bf16x2(h0, h1);
             }
           } else {
             uint32_t v[32];
@@ -503,7 +513,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              packed[ch * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+              packed[cl * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
         }
       }
@@ -519,27 +529,28 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       // 2-byte stores measured faster than paying for the shuffles.
       const int colg = c.j * 256 + 128 * static_cast<int>(rank) + col;
       if (!kUp && colg < N_out) {
-        uint16_t* dst = D + static_cast<int64_t>(c.row0) * N_out + colg;
+        uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + colg;
 #pragma unroll
-        for (int i = 0; i < S_TOK / 2; ++i) {
-          if (2 * i < c.rows) {
+        for (int i = 0; i < CH_PER * 16; ++i) {
+          if (tok0 + 2 * i < c.rows) {
             const uint32_t v = packed[i];
             dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
-            if (2 * i + 1 < c.rows) dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+            if (tok0 + 2 * i + 1 < c.rows)
+              dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
           }
         }
       }
       if (kUp && colg < N_out) {  // uniform across the warp (N_out % 128 == 0)
         const int odd = lane & 1;
         uint32_t* dst =
-            reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + odd) * N_out + (colg & ~1));
+            reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + tok0 + odd) * N_out + (colg & ~1));
 #pragma unroll
-        for (int i = 0; i < S_TOK / 2; ++i) {
-          if (2 * i < c.rows) {
+        for (int i = 0; i < CH_PER * 16; ++i) {
+          if (tok0 + 2 * i < c.rows) {
             const uint32_t mine = packed[i];
             const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
             const uint32_t v = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
-            if (2 * i + odd < c.rows) dst[static_cast<int64_t>(i) * N_out] = v;  // two rows = N_out words
+            if (tok0 + 2 * i + odd < c.rows) dst[static_cast<int64_t>(i) * N_out] = v;  // two rows = N_out words
           }
         }
       }
