@@ -385,7 +385,7 @@ def run_ours(args, world, rank, local):
     up_ms = statistics.mean(parts["up"])
     up_flops = 4.0 * T * k * H * I
     traffic = recorded_traffic("grouped_gemm_up") if workload == WORKLOAD else None
-    cpu_v, cpu_desc, cpu_cores, _ = cpu_oracle_sample(cfg, inp, seconds=12.0)
+    cpu_v, cpu_desc, cpu_cores, _ = cpu_oracle_sample(cfg, inp, seconds=15.0, max_tokens=cfg.T)
     counts = ws[v.counts - ws.data_ptr():v.counts - ws.data_ptr() + 4 * E].view(torch.int32).cpu().numpy()
     touched = int((counts > 0).sum())
     # algorithmic bytes of the up call: each touched expert's W_gate and W_up

@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
     // thread = TMEM lane = weight column `col` of this CTA's 128: it holds
-    // that column for every token of the window and writes it down the
-    // output rows
+    // that column for its warp's half of the window's tokens and writes it
+    // down those output rows
     const int q = warp & 3;                                   // TMEM lane quarter
     const int col = q * 32 + lane;
     constexpr int CH_PER = S_TOK / 32 / S_EPI_SPLIT;          // 32-token chunks per warp
