@@ -356,6 +356,23 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status after the breakdown")
     steps_ms = sum(e[0].elapsed_time(e[4]) for e in evs) / K
 
+    # ---------------- the dominant kernel alone: the gate/up GEMM on the rows
+    # the last step gathered (moe_grouped_gemm_up_rows), K launches between
+    # events on the launching stream
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        for _ in range(K):
+            if lib.moe_grouped_gemm_up_rows(sp, v.Xp, v.counts, v.off_pad, wg.data_ptr(), wu.data_ptr(), v.h,
+                                            ws.data_ptr(), sh):
+                raise RuntimeError("moe_grouped_gemm_up_rows failed")
+        g1.record(stream)
+    torch.cuda.synchronize(dev)
+    gemm_ms = g0.elapsed_time(g1) / K
+    if moe.last_device_status(ws, sh) != 0:
+        raise RuntimeError("device status after the GEMM timing")
+
     # ---------------- end to end: host buffers, copies inside the timed region
     # Every step copies its inputs (logits, X) from pinned host memory and its
     # output back.  The copies run on a second stream, double-buffered, so
@@ -417,24 +434,33 @@ def run_ours(args, world, rank, local):
     pk, pk_src = peaks()
     up_ms = statistics.mean(parts["up"])
     up_flops = 4.0 * T * k * H * I
-    traffic = recorded_traffic("grouped_gemm_up") if workload == WORKLOAD else None
+    traffic_call = recorded_traffic("grouped_gemm_up") if workload == WORKLOAD else None
+    traffic = recorded_traffic("grouped_gemm_window_kernel_up") if workload == WORKLOAD else None
     cpu_v, cpu_desc, cpu_cores, _ = cpu_oracle_sample(cfg, inp, seconds=15.0, max_tokens=cfg.T)
     counts = ws[v.counts - ws.data_ptr():v.counts - ws.data_ptr() + 4 * E].view(torch.int32).cpu().numpy()
     touched = int((counts > 0).sum())
-    # algorithmic bytes of the up call: each touched expert's W_gate and W_up
-    # once, each token row of X once, h written once
+    def roofline_of(alg_bytes, ms):
+        # the bound is the larger floor: bytes at the measured copy bandwidth
+        # vs FLOPs at the measured sustained bf16 rate
+        tflops = up_flops / (ms * 1e-3) / 1e12
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        extra = {"algorithmic_bytes_per_launch": alg_bytes, "algorithmic_flops_per_launch": up_flops,
+                 "us_per_launch": ms * 1e3, "hbm_frac": gbs / pk["hbm_gbs"],
+                 "tensor_frac_sustained": tflops / pk["bf16_tflops_sustained"],
+                 "tensor_frac_burst": tflops / pk["bf16_tflops"]}
+        if alg_bytes / pk["hbm_gbs"] / 1e9 >= up_flops / pk["bf16_tflops_sustained"] / 1e12:
+            return dict(extra, bound="hbm", achieved=gbs, peak=pk["hbm_gbs"], unit="GB/s",
+                        frac=gbs / pk["hbm_gbs"], peak_source="%s hbm_gbs" % pk_src)
+        return dict(extra, bound="tensor", achieved=tflops, peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
+                    frac=tflops / pk["bf16_tflops_sustained"], peak_source="%s bf16_tflops_sustained" % pk_src)
+
+    # the GEMM kernel: each touched expert's W_gate and W_up once, each
+    # gathered row once, h written once
+    gemm_bytes = touched * 2 * H * I * 2 + T * k * H * 2 + T * k * I * 2
+    # the up call (gather + GEMM): each token row of X once instead
     up_bytes = touched * 2 * H * I * 2 + T * H * 2 + T * k * I * 2
-    tflops = up_flops / (up_ms * 1e-3) / 1e12
-    gbs = up_bytes / (up_ms * 1e-3) / 1e9
-    # the roofline bound is the larger floor: bytes at the measured copy
-    # bandwidth vs FLOPs at the measured sustained bf16 rate
-    hbm_bound = up_bytes / pk["hbm_gbs"] / 1e9 >= up_flops / pk["bf16_tflops_sustained"] / 1e12
-    if hbm_bound:
-        roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / pk["hbm_gbs"], "peak_source": "%s hbm_gbs" % pk_src}
-    else:
-        roof = {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": tflops / pk["bf16_tflops_sustained"], "peak_source": "%s bf16_tflops_sustained" % pk_src}
+    roof = roofline_of(gemm_bytes, gemm_ms)
+    roof_call = roofline_of(up_bytes, up_ms)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3,
@@ -447,13 +473,11 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "per_kernel_us": {n: statistics.mean(vv) * 1e3 for n, vv in parts.items()},
         "step_by_step_us": steps_ms * 1e3,
-        "roofline": dict(roof, kernel="moe_grouped_gemm_up call (row gather + token-window CTA-pair "
-                                      "tcgen05 grouped GEMM)",
-                         traffic=traffic, algorithmic_bytes_per_launch=up_bytes,
-                         algorithmic_flops_per_launch=up_flops,
-                         hbm_frac=gbs / pk["hbm_gbs"],
-                         tensor_frac_sustained=tflops / pk["bf16_tflops_sustained"],
-                         tensor_frac_burst=tflops / pk["bf16_tflops"]),
+        "roofline": dict(roof, kernel="grouped_gemm_window_kernel<up> (token-window CTA-pair tcgen05 grouped "
+                                      "GEMM, timed through moe_grouped_gemm_up_rows)",
+                         traffic=traffic,
+                         up_call=dict(roof_call, kernel="moe_grouped_gemm_up call (row gather + the GEMM)",
+                                      traffic=traffic_call)),
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_cores, "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

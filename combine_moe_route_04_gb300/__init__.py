@@ -15,7 +15,8 @@ import os
 __all__ = ["MoEError", "MoEShape", "MoEViews", "lib_path", "load", "shape", "capacity",
            "workspace_size", "alloc_workspace", "workspace_init", "workspace_views",
            "last_device_status", "alloc_route_outputs", "moe_route", "moe_grouped_gemm_up",
-           "moe_grouped_gemm_down", "moe_combine", "moe_forward", "STATUS_NAMES", "EXPORTS"]
+           "moe_grouped_gemm_up_rows", "moe_grouped_gemm_down", "moe_combine", "moe_forward",
+           "STATUS_NAMES", "EXPORTS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
@@ -27,7 +28,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_S
 # every function include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_init",
            "moe_last_device_status", "moe_route", "moe_grouped_gemm_up", "moe_grouped_gemm_down",
-           "moe_combine", "moe_forward", "moe_workspace_views", "moe_route_noalloc"]
+           "moe_combine", "moe_forward", "moe_workspace_views", "moe_route_noalloc",
+           "moe_grouped_gemm_up_rows"]
 
 
 class MoEError(RuntimeError):
@@ -44,7 +46,7 @@ class MoEShape(ctypes.Structure):
 class MoEViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("topk_ids", "topk_w", "counts", "off_pad",
                                                 "block_expert", "num_blocks", "gather_idx",
-                                                "scatter_idx", "h", "Y")]
+                                                "scatter_idx", "h", "Y", "Xp")]
 
 
 _lib = None
@@ -83,6 +85,8 @@ def load():
     lib.moe_route_noalloc.argtypes = [S] + [P] * 10
     lib.moe_grouped_gemm_up.restype = st
     lib.moe_grouped_gemm_up.argtypes = [S] + [P] * 9
+    lib.moe_grouped_gemm_up_rows.restype = st
+    lib.moe_grouped_gemm_up_rows.argtypes = [S] + [P] * 8
     lib.moe_grouped_gemm_down.restype = st
     lib.moe_grouped_gemm_down.argtypes = [S] + [P] * 7
     lib.moe_combine.restype = st
@@ -249,6 +253,22 @@ def moe_grouped_gemm_up(s, X, scatter_idx, counts, off_pad, W_gate, W_up, h, ws,
             _dev_tensor(h, bf, mr * s.I, "h"),
             _dev_tensor(ws, torch.uint8, workspace_size(s), "ws")]
     _check(load().moe_grouped_gemm_up(ctypes.byref(s), *args, _stream(stream)), "moe_grouped_gemm_up")
+
+
+def moe_grouped_gemm_up_rows(s, Xp, counts, off_pad, W_gate, W_up, h, ws, stream=None):
+    """The gate/up GEMM on rows already in expert order (no row gather)."""
+    import torch
+    s = _shape_obj(s)
+    mb, mr = capacity(s)
+    bf = torch.bfloat16
+    args = [_dev_tensor(Xp, bf, mr * s.H, "Xp"),
+            _dev_tensor(counts, torch.int32, s.E, "counts"),
+            _dev_tensor(off_pad, torch.int32, s.E + 1, "off_pad"),
+            _dev_tensor(W_gate, bf, s.E * s.H * s.I, "W_gate"),
+            _dev_tensor(W_up, bf, s.E * s.H * s.I, "W_up"),
+            _dev_tensor(h, bf, mr * s.I, "h"),
+            _dev_tensor(ws, torch.uint8, workspace_size(s), "ws")]
+    _check(load().moe_grouped_gemm_up_rows(ctypes.byref(s), *args, _stream(stream)), "moe_grouped_gemm_up_rows")
 
 
 def moe_grouped_gemm_down(s, h, counts, off_pad, W_down, Y, ws, stream=None):

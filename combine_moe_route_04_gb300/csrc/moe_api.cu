@@ -92,6 +92,7 @@ Views views_of(const moe_shape& s, void* ws) {
   w.status = reinterpret_cast<uint32_t*>(b + L.status);
   w.chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   w.xp = reinterpret_cast<uint16_t*>(b + L.xp);
+  w.v.Xp = reinterpret_cast<moe_bf16*>(w.xp);
   w.v.topk_ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
   w.v.topk_w = reinterpret_cast<float*>(b + L.topk_w);
   w.v.counts = reinterpret_cast<int32_t*>(b + L.counts);
@@ -107,18 +108,26 @@ Views views_of(const moe_shape& s, void* ws) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, const int32_t* counts,
-                  const int32_t* off_pad, const uint16_t* Wg, const uint16_t* Wu,
-                  uint16_t* h, const Views& w, int num_sms, cudaStream_t st) {
+// The gate/up GEMM over rows already in expert order (Xp [max_rows][H]).
+moe_status run_up_rows(const moe_shape& s, const uint16_t* Xp, const int32_t* counts, const int32_t* off_pad,
+                       const uint16_t* Wg, const uint16_t* Wu, uint16_t* h, const Views& w, int num_sms,
+                       cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
-  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, w.status, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
-  if (!encode_bf16_2d(&m.a, w.xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
+  if (!encode_bf16_2d(&m.a, Xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
       !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
     return MOE_ERR_CUDA;
   return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), num_sms, st));
+}
+
+// Row gather into the workspace's Xp, then the GEMM over it.
+moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, const int32_t* counts,
+                  const int32_t* off_pad, const uint16_t* Wg, const uint16_t* Wu,
+                  uint16_t* h, const Views& w, int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, w.status, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return run_up_rows(s, w.xp, counts, off_pad, Wg, Wu, h, w, num_sms, st);
 }
 
 moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts, const int32_t* off_pad,
@@ -292,6 +301,23 @@ moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const 
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
   return run_up(*shape, X, scatter_idx, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), sms, s);
+}
+
+moe_status moe_grouped_gemm_up_rows(const moe_shape* shape, const moe_bf16* Xp, const int32_t* counts,
+                                    const int32_t* off_pad, const moe_bf16* W_gate, const moe_bf16* W_up,
+                                    moe_bf16* h, void* ws, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {Xp, counts, off_pad, W_gate, W_up, h, ws};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int sms = 0;
+  st = prepare_device(s, &sms);
+  if (st != MOE_OK) return st;
+  return run_up_rows(*shape, Xp, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), sms, s);
 }
 
 moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, const int32_t* counts,

@@ -166,6 +166,19 @@ moe_status moe_grouped_gemm_up(const moe_shape *shape, const moe_bf16 *X,
                                const moe_bf16 *W_up, moe_bf16 *h, void *ws,
                                moe_stream_t stream);
 
+/* Step 3 on rows already grouped by expert (for callers whose dispatch
+ * delivers them that way): the same GEMM and epilogue as
+ * moe_grouped_gemm_up, without the row gather.
+ *   Xp         [max_rows, H] bf16: row r holds the token of permuted row r
+ *              (the rows of expert e from off_pad[e], counts[e] of them;
+ *              padding rows are not read into any stored result)
+ *   counts, off_pad, W_gate, W_up, h: as for moe_grouped_gemm_up
+ *   ws         workspace (the tile counter, the status word) */
+moe_status moe_grouped_gemm_up_rows(const moe_shape *shape, const moe_bf16 *Xp,
+                                    const int32_t *counts, const int32_t *off_pad,
+                                    const moe_bf16 *W_gate, const moe_bf16 *W_up,
+                                    moe_bf16 *h, void *ws, moe_stream_t stream);
+
 /* Step 4: grouped down GEMM.
  *   h      [max_rows, I] bf16 (permuted rows), counts / off_pad from moe_route,
  *   W_down [E, I, H] bf16
@@ -207,6 +220,7 @@ typedef struct {
     int32_t *scatter_idx;
     moe_bf16 *h;
     moe_bf16 *Y;
+    moe_bf16 *Xp;   /* [max_rows, H]: the gathered token rows in expert order */
 } moe_views;
 
 moe_status moe_workspace_views(const moe_shape *shape, void *ws, moe_views *views);

@@ -1,6 +1,7 @@
-"""Per-kernel GPU parity: the grouped gate/up GEMM, the grouped down GEMM and
-the combine, each fed the oracle's own inputs (its route and, for down and
-combine, its h / Y), so an error is localised to one kernel.  Shapes span
+"""Per-kernel GPU parity: the grouped gate/up GEMM (with its row gather, and
+on rows already in expert order), the grouped down GEMM and the combine, each
+fed the oracle's own inputs (its route and, for down and combine, its h / Y),
+so an error is localised to one kernel.  Shapes span
 several row blocks and column tiles, ragged expert groups, an expert of
 exactly 128 and one of 129 rows, and empty experts."""
 import numpy as np
@@ -67,6 +68,15 @@ def test_grouped_gemms_and_combine(oracle_mod, name):
     assert moe.last_device_status(ws) == 0
     h_got = host_u16(h)[:r.num_blocks * 128]
     assert_rows_close(h_got[real], ref.h[real], "h")
+
+    # the same GEMM on rows already in expert order (no gather): Xp[r] = X[gather_idx[r]]
+    xp = np.zeros((mr, H), np.uint16)
+    xp[real] = x[r.gather_idx[real]]
+    h2 = torch.empty((mr, I), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_gemm_up_rows(s, to_dev_bf16(xp), d["counts"], d["off_pad"], to_dev_bf16(wg),
+                                 to_dev_bf16(wu), h2, ws)
+    assert moe.last_device_status(ws) == 0
+    assert np.array_equal(host_u16(h2)[real], h_got[real])
 
     # down GEMM on the oracle's h
     h_ref_dev = torch.zeros((mr, I), dtype=torch.bfloat16, device="cuda")

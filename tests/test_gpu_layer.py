@@ -52,7 +52,7 @@ def _view_arrays(moe, s, ws):
         "block_expert": grab(v.block_expert, mb, torch.int32)[:nb],
         "gather_idx": grab(v.gather_idx, mr, torch.int32)[:nb * 128],
         "scatter_idx": grab(v.scatter_idx, T * k, torch.int32).reshape(T, k),
-        "h_ptr": v.h, "Y_ptr": v.Y,
+        "h_ptr": v.h, "Y_ptr": v.Y, "Xp_ptr": v.Xp,
     }
 
 
@@ -89,6 +89,10 @@ def test_forward_small_full_oracle(oracle_mod, name):
     assert np.array_equal(v["topk_ids"], ref.route.topk_ids)
     assert np.array_equal(v["gather_idx"], ref.route.gather_idx)
     assert np.array_equal(v["scatter_idx"], ref.route.scatter_idx)
+    # the gathered rows the up GEMM read: Xp[r] = X[gather_idx[r]], bit for bit
+    real = np.nonzero(ref.route.gather_idx >= 0)[0]
+    xp = _rows_of(ws, v["Xp_ptr"], real, H)
+    assert np.array_equal(xp, inp["x"][ref.route.gather_idx[real]])
 
 
 def _sample_tokens(ref_route, T, rng, n_random=29):
