@@ -71,6 +71,7 @@ SMALL = {
     "single_token": ((1, 256, 256, 8, 2), 79),
     "k_equals_E": ((70, 256, 128, 4, 4), 80),
     "many_experts": ((96, 256, 128, 256, 16), 81),
+    "smallest_dims": ((50, 128, 128, 3, 2), 82),      # H = I = 128: the down tile is half outside, K = 4 stages
 }
 
 
