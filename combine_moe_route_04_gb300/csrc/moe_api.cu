@@ -116,7 +116,7 @@ moe_status run_up_rows(const moe_shape& s, const uint16_t* Xp, const int32_t* co
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
   if (!encode_bf16_2d(&m.a, Xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
-      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.d, h, mr, s.I, 128, 64))
+      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64))
     return MOE_ERR_CUDA;
   return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), num_sms, st));
 }
@@ -135,8 +135,7 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EI = static_cast<uint64_t>(s.E) * s.I;
-  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64) ||
-      !encode_bf16_2d(&m.d, Y, mr, s.H, 128, 64))
+  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
   return cuda_status(launch_gemm_down(s, m, Y, off_pad, counts, w.status, ws_sched_down(w.status), num_sms, st));

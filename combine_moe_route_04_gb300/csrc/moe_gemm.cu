@@ -1,15 +1,18 @@
 // moe_gemm.cu -- persistent, warp-specialised grouped GEMMs of the expert
 // layer on the sm_103a tensor cores (tcgen05 + TMEM + TMA), and the row
-// gather that feeds the gate/up GEMM.
+// gather that fills their input.
 //
 // What they compute ("通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §1: gate/up
 // GEMM -> SiLU -> down GEMM; "通算融合算子（三）：ThunderKittens 多卡编程与可融合的
-// GEMM 模板" §4: each 128-row block multiplies the weights of its own expert,
-// tasks visited expert by expert):
-//   up:   for each 128-row block b of expert e and each 128-column slice j,
-//         G = A_b Wg[e][:, j], U = A_b Wu[e][:, j]  (float32 in TMEM)
-//         h[b, j] = bf16(silu(G) * U)
-//   down: Y[b, j] = bf16(h_b Wd[e][:, j]) for 256-column slices j.
+// GEMM 模板" §4: rows grouped by expert, each group multiplies the weights of
+// its own expert, tasks visited expert by expert):
+//   up:   for each window A_w of expert e's rows (in permuted order) and each
+//         256-column weight slice j,
+//         G = A_w Wg[e][:, j], U = A_w Wu[e][:, j]  (float32 in TMEM)
+//         h[w, j] = bf16(silu(G) * U)
+//   down: Y[w, j] = bf16(h_w Wd[e][:, j]) for 256-column slices j.
+// The row gather (scatter_rows_kernel) writes X[t] to each of token t's k
+// permuted rows, reading every row of X once.
 //
 // Design (the roles and barrier lifetimes of "TIRx 与高性能GEMM (下)" Step 7,
 // and the two-CTA MMA of its Step 8, re-keyed to expert row windows):
@@ -23,6 +26,9 @@
 //   * an expert's rows are cut into equal windows so the tiles sharing a
 //     weight tile run in step and read it from L2 together; padding beyond
 //     the real rows costs at most 15 rows per window;
+//   * tiles: the down GEMM's clusters take them round-robin; the up GEMM's
+//     draw them from a counter in the workspace (see the tile scheduler
+//     below), in the same expert-major order;
 //   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its weight
 //     columns (two 32x64 boxes, 128-byte swizzle; the up GEMM loads W_gate
 //     and W_up) and its token rows (128x32, 64-byte swizzle) into a ring of
@@ -34,11 +40,10 @@
 //   * warps 2-9 of each CTA drain the accumulator (thread = weight column;
 //     two warps per 32-lane TMEM quarter, each taking half of the window's
 //     tokens) into registers, release it on CTA 0's accumulator-empty
-//     barrier, and
-//     write their column down the window's output rows (in the up GEMM
-//     neighbouring lanes swap token halves and store two columns of one
-//     token each).  The down GEMM double-buffers its
-//     256-column accumulators; the up GEMM's g | u fill TMEM.
+//     barrier, and write their column down the window's output rows (in the
+//     up GEMM neighbouring lanes swap token halves and store two columns of
+//     one token each).  The down GEMM double-buffers its 256-column
+//     accumulators; the up GEMM's g | u fill TMEM.
 // Every wait on an mbarrier is bounded; on a timeout the kernel records it in
 // the status word, the roles stop, in-flight copies and MMAs are drained
 // (bounded) and TMEM is freed before exit.
@@ -77,7 +82,7 @@ __device__ __forceinline__ bool vote_any_epi(bool flag) {
 }
 
 // ---------------------------------------------------------------------------
-// Token-window variant ("swap" orientation).  The weights are the M=256 MMA
+// Token-window ("swap") orientation.  The weights are the M=256 MMA
 // operand (CTA r holds 128 weight columns, N-major boxes read as an MN-major
 // A operand) and the expert's tokens are the N operand: a tile is one window
 // of up to 256 consecutive rows of one expert times 256 weight columns, and
@@ -92,8 +97,8 @@ __device__ __forceinline__ bool vote_any_epi(bool flag) {
 //         one accumulator set (the epilogue drain is short against K = H).
 //   down: one MMA per K step; two 256-column accumulators double-buffer the
 //         epilogue.
-// The epilogue writes each column's values down a 128-row box in shared
-// memory (a transpose on the way out) and TMA-stores it.
+// The epilogue holds one weight column for its share of the window's tokens
+// and writes it down the output rows (the transpose happens on the way out).
 constexpr int S_TOK = 256;                               // max tokens per window
 constexpr int S_TOK_BOX = 128;                           // token rows per TMA box (per CTA)
 constexpr int S_W_BYTES = 2 * B_BOX_BYTES;               // 8 KB: 32 k-rows x 128 weight columns
@@ -101,8 +106,9 @@ constexpr int S_T_BYTES = S_TOK_BOX * BK * 2;            // 8 KB: 128 token rows
 constexpr int S_THREADS = (2 + S_EPI_WARPS) * 32;        // producer, MMA, epilogue warps
 constexpr int S_GROUP_WINDOWS = 4;                       // L2 grouping of windows inside an expert
 constexpr int S_TILE_RING = 8;                           // tile indices in flight from the scheduler
-// readers of each tile index: CTA 0's MMA lane and 4 epilogue warps, CTA 1's
-// producer lane and 4 epilogue warps (CTA 0's producer lane is the scheduler)
+// readers of each tile index: CTA 0's MMA lane and its epilogue warps, CTA
+// 1's producer lane and its epilogue warps (CTA 0's producer lane is the
+// scheduler)
 constexpr int S_TILE_READERS = 1 + S_EPI_WARPS + 1 + S_EPI_WARPS;
 
 template <bool kUp>

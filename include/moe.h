@@ -136,8 +136,7 @@ moe_status moe_route(const moe_shape *shape, const float *logits,
  *     stream.  Every scratch entry a call reads is written earlier in the
  *     same call, so nothing needs clearing between calls.
  *   - The first call on a device looks up the scratch address on that device
- *     (a host-side query, no allocation); make that first call before any
- *     stream capture.
+ *     (a host-side query, no allocation) and caches it.
  *   - Kernel-side errors are not reported (there is no status word).
  * Arguments as moe_route, without ws. */
 moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
