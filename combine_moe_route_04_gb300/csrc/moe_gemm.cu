@@ -10,29 +10,31 @@
 //         256-column weight slice j,
 //         G = A_w Wg[e][:, j], U = A_w Wu[e][:, j]  (float32 in TMEM)
 //         h[w, j] = bf16(silu(G) * U)
-//   down: Y[w, j] = bf16(h_w Wd[e][:, j]) for 256-column slices j.
+//   down: Y[w, j] = bf16(h_w Wd[e][:, j]) for 512-column slices j.
 // The row gather (scatter_rows_kernel) writes X[t] to each of token t's k
 // permuted rows, reading every row of X once.
 //
 // Design (the roles and barrier lifetimes of "TIRx 与高性能GEMM (下)" Step 7,
 // and the two-CTA MMA of its Step 8, re-keyed to expert row windows):
-//   * a cluster of two CTAs on two SMs computes one tile = 256 weight
-//     columns x one window of an expert's rows with M=256 tcgen05.mma
-//     (cta_group::2).  The weights are the M operand: CTA r holds 128 weight
-//     columns (N-major boxes read as an MN-major A operand); the window's
-//     tokens are the N operand (N = real rows rounded up to 16, at most 256),
-//     CTA r supplying tokens [r N/2, (r+1) N/2).  Each CTA's TMEM holds its
-//     128 weight columns (lanes) for all N tokens (columns);
+//   * a cluster of two CTAs on two SMs computes one tile = one window of an
+//     expert's rows x 256 weight columns (up: of W_gate and of W_up) or 512
+//     (down), with M=256 tcgen05.mma (cta_group::2).  The weights are the M
+//     operand: per MMA CTA r holds 128 weight columns (N-major boxes read as
+//     an MN-major A operand); the window's tokens are the N operand (N = real
+//     rows rounded up to 16, at most 256), CTA r supplying tokens
+//     [r N/2, (r+1) N/2).  Each CTA's TMEM holds two accumulators of 128
+//     weight columns (lanes) x N tokens (columns), filled by two MMAs per K
+//     step that share the token rows;
 //   * an expert's rows are cut into equal windows so the tiles sharing a
 //     weight tile run in step and read it from L2 together; padding beyond
 //     the real rows costs at most 15 rows per window;
-//   * tiles: the down GEMM's clusters take them round-robin; the up GEMM's
-//     draw them from a counter in the workspace (see the tile scheduler
-//     below), in the same expert-major order;
+//   * tiles: each GEMM's clusters draw them from a counter in the workspace
+//     (see the tile scheduler below), in expert-major order;
 //   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its weight
-//     columns (two 32x64 boxes, 128-byte swizzle; the up GEMM loads W_gate
-//     and W_up) and its token rows (128x32, 64-byte swizzle) into a ring of
-//     9 (up) / 13 (down) stages; all loads complete on CTA 0's full barriers;
+//     columns (two 32x64 boxes per accumulator, 128-byte swizzle: the up
+//     GEMM loads W_gate and W_up, the down GEMM two neighbouring blocks of
+//     W_down) and its token rows (128x32, 64-byte swizzle) into a ring of 9
+//     stages of 24 KB; all loads complete on CTA 0's full barriers;
 //   * warp 1 allocates 512 TMEM columns in both CTAs; in CTA 0 one elected
 //     lane issues the MMAs (the up GEMM issues a W_gate and a W_up MMA per K
 //     step into accumulators g | u, so SiLU(g)*u meets in one thread) and
@@ -42,8 +44,7 @@
 //     tokens) into registers, release it on CTA 0's accumulator-empty
 //     barrier, and write their column down the window's output rows (in the
 //     up GEMM neighbouring lanes swap token halves and store two columns of
-//     one token each).  The down GEMM double-buffers its 256-column
-//     accumulators; the up GEMM's g | u fill TMEM.
+//     one token each).  The two accumulators fill TMEM (one set).
 // Every wait on an mbarrier is bounded; on a timeout the kernel records it in
 // the status word, the roles stop, in-flight copies and MMAs are drained
 // (bounded) and TMEM is freed before exit.
@@ -93,10 +94,13 @@ __device__ __forceinline__ bool vote_any_epi(bool flag) {
 // columns for their own 128 weight columns (TMEM lane = weight column).
 //   up:   two MMAs per K step, W_gate columns into accumulator g and the same
 //         W_up columns into accumulator u, so a thread owns g and u of one
-//         column for every token; h = SiLU(g) * u.  512 TMEM columns = g | u,
-//         one accumulator set (the epilogue drain is short against K = H).
-//   down: one MMA per K step; two 256-column accumulators double-buffer the
-//         epilogue.
+//         column for every token; h = SiLU(g) * u.
+//   down: two MMAs per K step into two accumulators of neighbouring
+//         128-column blocks of W_down (a 512-column tile per pair).
+// 512 TMEM columns = the two accumulators: one set, so the epilogue drain is
+// not overlapped with the next tile's MMAs (measured: double-buffering the
+// down GEMM's single 256-column accumulator instead was slower, its stages
+// then needing more shared-memory bandwidth than the data path has).
 // The epilogue holds one weight column for its share of the window's tokens
 // and writes it down the output rows (the transpose happens on the way out).
 constexpr int S_TOK = 256;                               // max tokens per window
@@ -111,11 +115,19 @@ constexpr int S_TILE_RING = 8;                           // tile indices in flig
 // scheduler)
 constexpr int S_TILE_READERS = 1 + S_EPI_WARPS + 1 + S_EPI_WARPS;
 
+// Both GEMMs run two 128-column accumulators per CTA that share each K
+// step's token rows: the up GEMM's gate and up columns, the down GEMM's two
+// neighbouring 128-column blocks (so a down tile is 512 weight columns, 256
+// per CTA).  A stage is 24 KB of loads for two MMAs, which keeps the
+// shared-memory traffic (TMA writes + MMA operand reads) below the data
+// path's bandwidth; the two accumulators fill TMEM, so there is one
+// accumulator set and the epilogue drain is not overlapped.
 template <bool kUp>
 struct SwapCfg {
-  static constexpr int STAGE_BYTES = (kUp ? 2 : 1) * S_W_BYTES + S_T_BYTES;  // up 24 KB, down 16 KB
-  static constexpr int STAGES = kUp ? 9 : 13;
-  static constexpr int NBUF = kUp ? 1 : 2;               // accumulator sets in TMEM
+  static constexpr int TILE_COLS = kUp ? 256 : 512;      // output columns per tile
+  static constexpr int STAGE_BYTES = 2 * S_W_BYTES + S_T_BYTES;  // 24 KB
+  static constexpr int STAGES = 9;
+  static constexpr int NBUF = 1;                         // accumulator sets in TMEM
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1 + 2 * S_TILE_RING;
   static constexpr int WIN_OFF = BAR_OFF + NUM_BARS * 8 + 16;
@@ -237,10 +249,6 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                                int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status,
                                uint32_t* __restrict__ sched) {
   using C = SwapCfg<kUp>;
-  // the up GEMM draws its tiles dynamically (its windows differ in size and
-  // there are few tiles per cluster); the down GEMM, with many short tiles,
-  // keeps the static round-robin order
-  constexpr bool kDyn = kUp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStage = smem;
@@ -326,7 +334,6 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   const int total_tiles = NT * s_win_off[E];
   const int KB = K / BK;
   const int nclusters = gridDim.x >> 1;
-  const int cluster_id = blockIdx.x >> 1;
   const uint32_t full0 = map_to_cta(full, 0);
   const uint32_t tempty0 = map_to_cta(tempty, 0);
   const uint32_t rempty0 = map_to_cta(ring.empty, 0);
@@ -339,21 +346,19 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       uint32_t it = 0;
       bool stop = false;
       // CTA 0 draws the pair's tiles and publishes them; CTA 1 reads them
-      int tile = cluster_id;
-      if (kDyn) {
-        if (rank == 0) {
-          tile = draw_tile(sched, total_tiles, nclusters, status);
-          stop = !ring_put(ring, 0, tile, abort_flag, status);
-        } else {
-          tile = ring_take(ring, 0, rank, rempty0, true, abort_flag, status);
-        }
+      int tile;
+      if (rank == 0) {
+        tile = draw_tile(sched, total_tiles, nclusters, status);
+        stop = !ring_put(ring, 0, tile, abort_flag, status);
+      } else {
+        tile = ring_take(ring, 0, rank, rempty0, true, abort_flag, status);
       }
       for (uint32_t n = 0; !stop && tile >= 0 && tile < total_tiles; ++n) {
         // CTA 0 draws the next tile now without waiting for the value, and
         // publishes it halfway through this tile's loads
-        const uint32_t raw_next = kDyn && rank == 0 ? atomicAdd(sched, 1u) : 0u;
-        int next = tile + nclusters;
-        bool published = !kDyn || rank != 0;
+        const uint32_t raw_next = rank == 0 ? atomicAdd(sched, 1u) : 0u;
+        int next = total_tiles;
+        bool published = rank != 0;
         auto publish = [&]() {
           next = raw_next < static_cast<uint32_t>(total_tiles + nclusters) ? static_cast<int>(raw_next) : total_tiles;
           if (next != static_cast<int>(raw_next)) record_status(status, kStatusBounds);
@@ -364,7 +369,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         if (!c.ok) record_status(status, kStatusBounds);
         const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
         const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
-        const int n0 = c.j * 256 + 128 * static_cast<int>(rank);       // its first weight column
+        const int n0 = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank);  // first weight column
         for (int kb = 0; c.ok && kb < KB; ++kb, ++it) {
           if (!published && kb == KB / 2 && !publish()) {
             stop = true;
@@ -382,17 +387,20 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           const int k0 = c.e * K + kb * BK;
           tma_load_2d_pair(st, &tmW0, fb, n0, k0, pol_w);
           tma_load_2d_pair(st + B_BOX_BYTES, &tmW0, fb, n0 + 64, k0, pol_w);
-          if (kUp) {
+          if (kUp) {  // the same columns of W_up
             tma_load_2d_pair(st + S_W_BYTES, &tmW1, fb, n0, k0, pol_w);
             tma_load_2d_pair(st + S_W_BYTES + B_BOX_BYTES, &tmW1, fb, n0 + 64, k0, pol_w);
+          } else {  // the CTA's next 128 columns of W_down
+            tma_load_2d_pair(st + S_W_BYTES, &tmW0, fb, n0 + 128, k0, pol_w);
+            tma_load_2d_pair(st + S_W_BYTES + B_BOX_BYTES, &tmW0, fb, n0 + 192, k0, pol_w);
           }
-          tma_load_2d_pair(st + (kUp ? 2 : 1) * S_W_BYTES, &tmT, fb, kb * BK, trow, pol_t);
+          tma_load_2d_pair(st + 2 * S_W_BYTES, &tmT, fb, kb * BK, trow, pol_t);
         }
         if (stop) break;
         if (!published && !publish()) break;
-        tile = !kDyn || rank == 0 ? next : ring_take(ring, n + 1, rank, rempty0, true, abort_flag, status);
+        tile = rank == 0 ? next : ring_take(ring, n + 1, rank, rempty0, true, abort_flag, status);
       }
-      if (kDyn && rank == 0) {
+      if (rank == 0) {
         // this cluster has drawn its last index; the last cluster to get here
         // clears the counter for the next launch
         __threadfence();
@@ -418,15 +426,14 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       uint32_t tcount = 0;
       bool stop = false;
       for (uint32_t n = 0; !stop; ++n) {
-        const int tile = kDyn ? ring_take(ring, n, rank, rempty0, true, abort_flag, status)
-                              : cluster_id + static_cast<int>(n) * nclusters;
+        const int tile = ring_take(ring, n, rank, rempty0, true, abort_flag, status);
         if (tile < 0 || tile >= total_tiles) break;
         const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
         if (!c.ok) continue;
         const uint32_t N = static_cast<uint32_t>(((c.rows + 15) / 16) * 16);
         const uint32_t idesc = idesc_base | ((N >> 3) << 17);
-        const uint32_t a = C::NBUF == 2 ? (tcount & 1u) : 0u;
-        const uint32_t aph = C::NBUF == 2 ? ((tcount >> 1) & 1u) : (tcount & 1u);
+        const uint32_t a = 0;               // one accumulator set (g | u, or the two blocks)
+        const uint32_t aph = tcount & 1u;
         if (!mbar_wait(&tempty[a], aph ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * ACC_COLS;
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t st = smem_u32(sStage + s * C::STAGE_BYTES);
-          const uint32_t tk = st + (kUp ? 2 : 1) * S_W_BYTES;
+          const uint32_t tk = st + 2 * S_W_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A (weights, this CTA's 128 columns): MN-major, 128-byte swizzle,
@@ -449,8 +456,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             const uint64_t bdesc = smem_desc(tk + kk * 32, 16, 512, kSwizzle64B);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             tc_mma_f16_pair(d, smem_desc(st + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B), bdesc, idesc, acc);
-            if (kUp)
-              tc_mma_f16_pair(d + 256, smem_desc(st + S_W_BYTES + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B),
+            tc_mma_f16_pair(d + 256, smem_desc(st + S_W_BYTES + kk * 2048, B_BOX_BYTES, 1024, kSwizzle128B),
                               bdesc, idesc, acc);
           }
           tc_commit_pair(&empty[s], 0x3);
@@ -476,23 +482,21 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     const int tok0 = ch0 * 32;                                // ... and first token
     uint32_t tcount = 0;
     for (uint32_t n = 0;; ++n) {
-      int tile = cluster_id + static_cast<int>(n) * nclusters;
-      if (kDyn) {
-        tile = ring_take(ring, n, rank, rempty0, false, abort_flag, status);
-        __syncwarp();
-        if (lane == 0) ring_release(ring, n, rank, rempty0);
-        if (vote_any_epi(tile < 0)) break;
-      }
+      const int tile = ring_take(ring, n, rank, rempty0, false, abort_flag, status);
+      __syncwarp();
+      if (lane == 0) ring_release(ring, n, rank, rempty0);
+      if (vote_any_epi(tile < 0)) break;
       if (tile >= total_tiles) break;
       const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
       if (!c.ok) continue;
-      const uint32_t a = C::NBUF == 2 ? (tcount & 1u) : 0u;
-      const uint32_t aph = C::NBUF == 2 ? ((tcount >> 1) & 1u) : (tcount & 1u);
+      const uint32_t a = 0;
+      const uint32_t aph = tcount & 1u;
       const bool ok = mbar_wait(&tfull[a], aph, abort_flag, status);
       if (vote_any_epi(!ok)) break;
       tc_fence_after();
       const int nchunks = (c.rows + 31) / 32;       // 32-token TMEM column chunks holding real rows
       uint32_t packed[CH_PER * 16];                 // bf16 pairs (token tok0+2i, +1) of this column
+      uint32_t packed1[kUp ? 1 : CH_PER * 16];      // down: the second accumulator's column
       const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
       for (int cl = 0; cl < CH_PER; ++cl) {
@@ -513,13 +517,19 @@ __global__ void __launch_bounds__(S_THREADS, 1)
               const float h1 = g1 * __fdividef(1.0f, 1.0f + __expf(-g1)) * u1;
               packed[cl * 16 + i] = pack_bf16x2(h0, h1);
             }
-          } else {
+          } else {  // down: one accumulator at a time (register pressure)
             uint32_t v[32];
             tmem_ld_32x32b_x32(tbase + ch * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               packed[cl * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            tmem_ld_32x32b_x32(tbase + 256 + ch * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed1[(cl * 16 + i) % (sizeof(packed1) / 4)] =
+                  pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
         }
       }
@@ -527,19 +537,30 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
       ++tcount;
-      // out[row0 + t][j*256 + 128 rank + col] for the window's real rows.
+      // out[row0 + t][tile columns + col] for the window's real rows.
       // Up GEMM: neighbouring lanes (columns 2m, 2m+1) swap halves of their
       // token pairs, so the even lane stores token 2i and the odd lane token
       // 2i+1, each as two adjacent columns (4 bytes): half as many stores.
-      // Down GEMM (short tiles, double-buffered): one column per lane and
-      // 2-byte stores measured faster than paying for the shuffles.
-      const int colg = c.j * 256 + 128 * static_cast<int>(rank) + col;
+      // Down GEMM: one column per lane per accumulator, 2-byte stores.
+      const int colg = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank) + col;
       if (!kUp && colg < N_out) {
         uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + colg;
 #pragma unroll
         for (int i = 0; i < CH_PER * 16; ++i) {
           if (tok0 + 2 * i < c.rows) {
             const uint32_t v = packed[i];
+            dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
+            if (tok0 + 2 * i + 1 < c.rows)
+              dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+          }
+        }
+      }
+      if (!kUp && colg + 128 < N_out) {  // the second accumulator: 128 columns further
+        uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + colg + 128;
+#pragma unroll
+        for (int i = 0; i < CH_PER * 16; ++i) {
+          if (tok0 + 2 * i < c.rows) {
+            const uint32_t v = packed1[i % (sizeof(packed1) / 4)];
             dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
             if (tok0 + 2 * i + 1 < c.rows)
               dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
@@ -633,10 +654,10 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
-  // 256 weight columns per tile (up: I % 256 == 0 keeps gate/up slices whole;
-  // down: the last tile of an H % 256 == 128 output is half outside, TMA
-  // zero-fills those weight columns and the store is skipped)
-  const int NT = kUp ? (s.I + 255) / 256 : (s.H + 255) / 256;
+  // 256 (up) / 512 (down) weight columns per tile; a last tile that reaches
+  // past I or H is partly outside: TMA zero-fills those weight columns and
+  // their stores are skipped
+  const int NT = kUp ? (s.I + 255) / 256 : (s.H + C::TILE_COLS - 1) / C::TILE_COLS;
   const int K = kUp ? s.H : s.I;
   const int64_t T_k = static_cast<int64_t>(s.T) * s.k;
   const int64_t max_windows = T_k / S_TOK + (s.E < T_k ? s.E : T_k);  // sum_e ceil(c_e / 256)
