@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       for (int cl = 0; cl < CH_PER; ++cl) {
         const int ch = ch0 + cl;
         if (ch < nchunks) {
-          if (kUp) {
+          if constexpr (kUp) {
             uint32_t gv[32], uv[32];
             tmem_ld_32x32b_x32(tbase + ch * 32, gv);
             tmem_ld_32x32b_x32(tbase + 256 + ch * 32, uv);
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              packed1[(cl * 16 + i) % (sizeof(packed1) / 4)] =
+              packed1[cl * 16 + i] =
                   pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
         }
@@ -543,31 +543,25 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       // 2i+1, each as two adjacent columns (4 bytes): half as many stores.
       // Down GEMM: one column per lane per accumulator, 2-byte stores.
       const int colg = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank) + col;
-      if (!kUp && colg < N_out) {
-        uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + colg;
+      if constexpr (!kUp) {
+        // one accumulator's column down the rows; a column past N_out (a
+        // last tile partly outside) is skipped, uniformly across the warp
+        auto store_column = [&](const uint32_t (&pk)[CH_PER * 16], int cg) {
+          if (cg >= N_out) return;
+          uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + cg;
 #pragma unroll
-        for (int i = 0; i < CH_PER * 16; ++i) {
-          if (tok0 + 2 * i < c.rows) {
-            const uint32_t v = packed[i];
-            dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
-            if (tok0 + 2 * i + 1 < c.rows)
-              dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+          for (int i = 0; i < CH_PER * 16; ++i) {
+            if (tok0 + 2 * i < c.rows) {
+              const uint32_t v = pk[i];
+              dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
+              if (tok0 + 2 * i + 1 < c.rows)
+                dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+            }
           }
-        }
-      }
-      if (!kUp && colg + 128 < N_out) {  // the second accumulator: 128 columns further
-        uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + colg + 128;
-#pragma unroll
-        for (int i = 0; i < CH_PER * 16; ++i) {
-          if (tok0 + 2 * i < c.rows) {
-            const uint32_t v = packed1[i % (sizeof(packed1) / 4)];
-            dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
-            if (tok0 + 2 * i + 1 < c.rows)
-              dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
-          }
-        }
-      }
-      if (kUp && colg < N_out) {  // uniform across the warp (N_out % 128 == 0)
+        };
+        store_column(packed, colg);
+        store_column(packed1, colg + 128);  // the second accumulator: 128 columns further
+      } else if (colg < N_out) {            // uniform across the warp (N_out % 128 == 0)
         const int odd = lane & 1;
         uint32_t* dst =
             reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + tok0 + odd) * N_out + (colg & ~1));
