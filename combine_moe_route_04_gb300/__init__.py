@@ -14,9 +14,9 @@ import os
 
 __all__ = ["MoEError", "MoEShape", "MoEViews", "lib_path", "load", "shape", "capacity",
            "workspace_size", "alloc_workspace", "workspace_init", "workspace_views",
-           "last_device_status", "alloc_route_outputs", "moe_route", "moe_grouped_gemm_up",
-           "moe_grouped_gemm_up_rows", "moe_grouped_gemm_down", "moe_combine", "moe_forward",
-           "STATUS_NAMES", "EXPORTS"]
+           "last_device_status", "check_wait_timeout", "alloc_route_outputs", "moe_route",
+           "moe_grouped_gemm_up", "moe_grouped_gemm_up_rows", "moe_grouped_gemm_down", "moe_combine",
+           "moe_forward", "STATUS_NAMES", "EXPORTS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_S
 EXPORTS = ["moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_init",
            "moe_last_device_status", "moe_route", "moe_grouped_gemm_up", "moe_grouped_gemm_down",
            "moe_combine", "moe_forward", "moe_workspace_views", "moe_route_noalloc",
-           "moe_grouped_gemm_up_rows"]
+           "moe_grouped_gemm_up_rows", "moe_check_wait_timeout"]
 
 
 class MoEError(RuntimeError):
@@ -79,6 +79,8 @@ def load():
     lib.moe_workspace_views.argtypes = [S, P, ctypes.POINTER(MoEViews)]
     lib.moe_last_device_status.restype = st
     lib.moe_last_device_status.argtypes = [P, P]
+    lib.moe_check_wait_timeout.restype = st
+    lib.moe_check_wait_timeout.argtypes = [P, P]
     lib.moe_route.restype = st
     lib.moe_route.argtypes = [S] + [P] * 11
     lib.moe_route_noalloc.restype = st
@@ -177,6 +179,12 @@ def workspace_views(s, ws) -> MoEViews:
 def last_device_status(ws, stream=None) -> int:
     """Synchronises the stream and returns (and clears) the kernels' status."""
     return load().moe_last_device_status(_ptr(ws), _stream(stream))
+
+
+def check_wait_timeout(ws, stream=None) -> None:
+    """Launches the diagnostic kernel whose bounded wait runs out (about 2 s);
+    the next last_device_status(ws) reports MOE_ERR_TIMEOUT."""
+    _check(load().moe_check_wait_timeout(_ptr(ws), _stream(stream)), "moe_check_wait_timeout")
 
 
 def alloc_route_outputs(s, device="cuda") -> dict:

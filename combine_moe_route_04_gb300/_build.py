@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_combine.cu"]
+SOURCES = ["moe_api.cu", "moe_route.cu", "moe_gemm.cu", "moe_combine.cu", "moe_check.cu"]
 HEADERS = ["moe_device.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -266,6 +266,15 @@ moe_status moe_last_device_status(void* ws, moe_stream_t stream) {
   return MOE_OK;
 }
 
+moe_status moe_check_wait_timeout(void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  moe_status st = prepare_device(s, nullptr);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_wait_timeout(static_cast<uint32_t*>(ws), s));
+}
+
 moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_ids, float* topk_w,
                      int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
                      int32_t* gather_idx, int32_t* scatter_idx, void* ws, moe_stream_t stream) {

@@ -96,6 +96,10 @@ cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t*
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
                            const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);
 
+// Diagnostic: one thread waits on an mbarrier that nothing arrives on, through
+// the library's bounded wait; records kStatusTimeout after kWaitLimitNs.
+cudaError_t launch_wait_timeout(uint32_t* status, cudaStream_t st);
+
 // Tensor-map encoding through the driver entry point (no link-time libcuda).
 // rows x cols bf16 row-major, box = box_cols (inner) x box_rows; the swizzle
 // span equals the box's inner extent in bytes (64 or 128).

@@ -98,6 +98,16 @@ moe_status moe_workspace_init(const moe_shape *shape, void *ws, moe_stream_t str
  * last call (MOE_OK if none) and clears it. */
 moe_status moe_last_device_status(void *ws, moe_stream_t stream);
 
+/* Diagnostic for the kernels' bounded waits: launches one thread that waits
+ * on an mbarrier nothing arrives on, through the same bounded wait as every
+ * pipeline of the library.  After the wait limit (2 s) the kernel records a
+ * timeout in the status word at the start of `ws` (a workspace, or any 16-byte
+ * aligned device buffer of at least 4 bytes whose first word is the status
+ * word) and returns; the GPU is not faulted.  The next
+ * moe_last_device_status(ws) returns MOE_ERR_TIMEOUT.  Asynchronous like the
+ * step calls; the stream is busy for about 2 s. */
+moe_status moe_check_wait_timeout(void *ws, moe_stream_t stream);
+
 /* Steps 1-2: routing, histogram, padded block table and permutation.
  *   logits       [T, E]  float32 (finite values)
  *   topk_ids     [T, k]  int32  out: picked experts, slot order
