@@ -473,13 +473,14 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
     // thread = TMEM lane = weight column `col` of this CTA's 128: it holds
-    // that column for its warp's half of the window's tokens and writes it
+    // that column for its warp's share of the window's tokens and writes it
     // down those output rows
     const int q = warp & 3;                                   // TMEM lane quarter
     const int col = q * 32 + lane;
-    constexpr int CH_PER = S_TOK / 32 / S_EPI_SPLIT;          // 32-token chunks per warp
-    const int ch0 = ((warp - 2) / 4) * CH_PER;                // this warp's first chunk
-    const int tok0 = ch0 * 32;                                // ... and first token
+    constexpr int CH_PER = S_TOK / 32 / S_EPI_SPLIT;          // 32-token chunks per warp (at most)
+    // the quarter's warps take its 32-token chunks in turn (chunk half,
+    // half + S_EPI_SPLIT, ...), so a short window still splits evenly
+    const int half = (warp - 2) / 4;
     uint32_t tcount = 0;
     for (uint32_t n = 0;; ++n) {
       const int tile = ring_take(ring, n, rank, rempty0, false, abort_flag, status);
@@ -495,18 +496,28 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       if (vote_any_epi(!ok)) break;
       tc_fence_after();
       const int nchunks = (c.rows + 31) / 32;       // 32-token TMEM column chunks holding real rows
-      uint32_t packed[CH_PER * 16];                 // bf16 pairs (token tok0+2i, +1) of this column
+      const int mine = nchunks > half ? (nchunks - half + S_EPI_SPLIT - 1) / S_EPI_SPLIT : 0;
+      // the accumulator is free once this warp's last TMEM load has landed:
+      // every warp arrives then, before converting that chunk
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
+      };
+      if (mine == 0) release();
+      uint32_t packed[CH_PER * 16];                 // bf16 pairs (token 2i, 2i+1 of chunk cl) of this column
       uint32_t packed1[kUp ? 1 : CH_PER * 16];      // down: the second accumulator's column
       const uint32_t tbase = tmem_base + a * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
       for (int cl = 0; cl < CH_PER; ++cl) {
-        const int ch = ch0 + cl;
-        if (ch < nchunks) {
+        const int ch = half + S_EPI_SPLIT * cl;
+        if (cl < mine) {
           if constexpr (kUp) {
             uint32_t gv[32], uv[32];
             tmem_ld_32x32b_x32(tbase + ch * 32, gv);
             tmem_ld_32x32b_x32(tbase + 256 + ch * 32, uv);
             tmem_ld_wait();
+            if (cl == mine - 1) release();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
@@ -526,6 +537,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
               packed[cl * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             tmem_ld_32x32b_x32(tbase + 256 + ch * 32, v);
             tmem_ld_wait();
+            if (cl == mine - 1) release();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               packed1[cl * 16 + i] =
@@ -533,9 +545,6 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * a);
       ++tcount;
       // out[row0 + t][tile columns + col] for the window's real rows.
       // Up GEMM: neighbouring lanes (columns 2m, 2m+1) swap halves of their
@@ -548,14 +557,19 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         // last tile partly outside) is skipped, uniformly across the warp
         auto store_column = [&](const uint32_t (&pk)[CH_PER * 16], int cg) {
           if (cg >= N_out) return;
-          uint16_t* dst = D + static_cast<int64_t>(c.row0 + tok0) * N_out + cg;
+          // chunk cl starts S_EPI_SPLIT * 32 * cl tokens after the warp's first
+          uint16_t* dst = D + static_cast<int64_t>(c.row0 + half * 32) * N_out + cg;
+          const int rem = c.rows - half * 32;
 #pragma unroll
-          for (int i = 0; i < CH_PER * 16; ++i) {
-            if (tok0 + 2 * i < c.rows) {
-              const uint32_t v = pk[i];
-              dst[static_cast<int64_t>(2 * i) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
-              if (tok0 + 2 * i + 1 < c.rows)
-                dst[static_cast<int64_t>(2 * i + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+          for (int cl = 0; cl < CH_PER; ++cl) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = S_EPI_SPLIT * 32 * cl + 2 * i;
+              if (t < rem) {
+                const uint32_t v = pk[cl * 16 + i];
+                dst[static_cast<int64_t>(t) * N_out] = static_cast<uint16_t>(v & 0xFFFFu);
+                if (t + 1 < rem) dst[static_cast<int64_t>(t + 1) * N_out] = static_cast<uint16_t>(v >> 16);
+              }
             }
           }
         };
@@ -564,14 +578,19 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       } else if (colg < N_out) {            // uniform across the warp (N_out % 128 == 0)
         const int odd = lane & 1;
         uint32_t* dst =
-            reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + tok0 + odd) * N_out + (colg & ~1));
+            reinterpret_cast<uint32_t*>(D + static_cast<int64_t>(c.row0 + half * 32 + odd) * N_out + (colg & ~1));
+        const int rem = c.rows - half * 32;
 #pragma unroll
-        for (int i = 0; i < CH_PER * 16; ++i) {
-          if (tok0 + 2 * i < c.rows) {
-            const uint32_t mine = packed[i];
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            const uint32_t v = odd ? __byte_perm(other, mine, 0x7632) : __byte_perm(mine, other, 0x5410);
-            if (tok0 + 2 * i + odd < c.rows) dst[static_cast<int64_t>(i) * N_out] = v;  // two rows = N_out words
+        for (int cl = 0; cl < CH_PER; ++cl) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = S_EPI_SPLIT * 32 * cl + 2 * i;
+            if (t < rem) {  // uniform across the warp
+              const uint32_t v_mine = packed[cl * 16 + i];
+              const uint32_t other = __shfl_xor_sync(0xffffffffu, v_mine, 1);
+              const uint32_t v = odd ? __byte_perm(other, v_mine, 0x7632) : __byte_perm(v_mine, other, 0x5410);
+              if (t + odd < rem) dst[static_cast<int64_t>(t / 2) * N_out] = v;  // two rows = N_out words
+            }
           }
         }
       }
