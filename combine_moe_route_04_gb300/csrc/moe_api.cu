@@ -82,6 +82,7 @@ struct Views {
   uint32_t* status;
   int32_t* chunk_counts;
   uint16_t* xp;
+  uint32_t* win_done;
   moe_views v;
 };
 
@@ -92,6 +93,7 @@ Views views_of(const moe_shape& s, void* ws) {
   w.status = reinterpret_cast<uint32_t*>(b + L.status);
   w.chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   w.xp = reinterpret_cast<uint16_t*>(b + L.xp);
+  w.win_done = reinterpret_cast<uint32_t*>(b + L.win_done);
   w.v.Xp = reinterpret_cast<moe_bf16*>(w.xp);
   w.v.topk_ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
   w.v.topk_w = reinterpret_cast<float*>(b + L.topk_w);
@@ -109,36 +111,40 @@ Views views_of(const moe_shape& s, void* ws) {
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // The gate/up GEMM over rows already in expert order (Xp [max_rows][H]).
+// win_done: nullptr, or the forward's per-window counters (see launch_gemm_up).
 moe_status run_up_rows(const moe_shape& s, const uint16_t* Xp, const int32_t* counts, const int32_t* off_pad,
-                       const uint16_t* Wg, const uint16_t* Wu, uint16_t* h, const Views& w, int num_sms,
-                       cudaStream_t st) {
+                       const uint16_t* Wg, const uint16_t* Wu, uint16_t* h, const Views& w, uint32_t* win_done,
+                       int num_sms, cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
   if (!encode_bf16_2d(&m.a, Xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
       !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64))
     return MOE_ERR_CUDA;
-  return cuda_status(launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), num_sms, st));
+  return cuda_status(
+      launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), win_done, num_sms, st));
 }
 
 // Row gather into the workspace's Xp, then the GEMM over it.
 moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, const int32_t* counts,
                   const int32_t* off_pad, const uint16_t* Wg, const uint16_t* Wu,
-                  uint16_t* h, const Views& w, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, w.status, st);
+                  uint16_t* h, const Views& w, uint32_t* win_done, int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, win_done, w.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return run_up_rows(s, w.xp, counts, off_pad, Wg, Wu, h, w, num_sms, st);
+  return run_up_rows(s, w.xp, counts, off_pad, Wg, Wu, h, w, win_done, num_sms, st);
 }
 
 moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts, const int32_t* off_pad,
-                    const uint16_t* Wd, uint16_t* Y, const Views& w, int num_sms, cudaStream_t st) {
+                    const uint16_t* Wd, uint16_t* Y, const Views& w, uint32_t* win_done, int num_sms,
+                    cudaStream_t st) {
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EI = static_cast<uint64_t>(s.E) * s.I;
   if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
-  return cuda_status(launch_gemm_down(s, m, Y, off_pad, counts, w.status, ws_sched_down(w.status), num_sms, st));
+  return cuda_status(
+      launch_gemm_down(s, m, Y, off_pad, counts, w.status, ws_sched_down(w.status), win_done, num_sms, st));
 }
 
 }  // namespace
@@ -171,6 +177,7 @@ WsLayout ws_layout(const moe_shape& s) {
   L.scatter_idx = take(T * k * 4);
   L.h = take(mr * static_cast<size_t>(s.I) * 2);
   L.y = take(mr * static_cast<size_t>(s.H) * 2);
+  L.win_done = take(static_cast<size_t>(max_windows_of(s)) * 4);
   L.total = off;
   return L;
 }
@@ -308,7 +315,7 @@ moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const 
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_up(*shape, X, scatter_idx, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), sms, s);
+  return run_up(*shape, X, scatter_idx, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), nullptr, sms, s);
 }
 
 moe_status moe_grouped_gemm_up_rows(const moe_shape* shape, const moe_bf16* Xp, const int32_t* counts,
@@ -325,7 +332,7 @@ moe_status moe_grouped_gemm_up_rows(const moe_shape* shape, const moe_bf16* Xp, 
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_up_rows(*shape, Xp, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), sms, s);
+  return run_up_rows(*shape, Xp, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), nullptr, sms, s);
 }
 
 moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, const int32_t* counts,
@@ -342,7 +349,7 @@ moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, cons
   int sms = 0;
   st = prepare_device(s, &sms);
   if (st != MOE_OK) return st;
-  return run_down(*shape, h, counts, off_pad, W_down, Y, views_of(*shape, ws), sms, s);
+  return run_down(*shape, h, counts, off_pad, W_down, Y, views_of(*shape, ws), nullptr, sms, s);
 }
 
 moe_status moe_combine(const moe_shape* shape, const moe_bf16* Y, const int32_t* scatter_idx, const float* topk_w,
@@ -381,9 +388,10 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   if (launch_route(sh, logits, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
                    v.gather_idx, v.scatter_idx, w.chunk_counts, w.status, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = run_up(sh, X, v.scatter_idx, v.counts, v.off_pad, W_gate, W_up, v.h, w, sms, s);
+  // the down GEMM starts on each token window as soon as its h rows are in
+  st = run_up(sh, X, v.scatter_idx, v.counts, v.off_pad, W_gate, W_up, v.h, w, w.win_done, sms, s);
   if (st != MOE_OK) return st;
-  st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, sms, s);
+  st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, w.win_done, sms, s);
   if (st != MOE_OK) return st;
   return cuda_status(launch_combine(sh, v.Y, v.scatter_idx, v.topk_w, out, w.status, s));
 }

@@ -102,6 +102,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Waits until *ctr >= target, read with acquire at GPU scope, then orders
+// this thread's later async-proxy (TMA) reads of global memory after the
+// writes the counter published.  Gives up like mbar_wait, and also as soon as
+// the status word holds an error (the producer of the count may have stopped
+// on it; that error is the one reported).
+__device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint32_t target, volatile int* abort,
+                                                      uint32_t* status) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if (*abort) return false;
+    if (status != nullptr && *reinterpret_cast<volatile uint32_t*>(status) != 0u) {
+      *abort = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_status(status, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(128);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel of the library starts with launch_dependents (the next kernel
 // may be scheduled once every CTA of this one has started) and calls wait

@@ -104,6 +104,7 @@ __device__ __forceinline__ bool vote_any_epi(bool flag) {
 // The epilogue holds one weight column for its share of the window's tokens
 // and writes it down the output rows (the transpose happens on the way out).
 constexpr int S_TOK = 256;                               // max tokens per window
+static_assert(S_TOK == kWindowRows, "window size shared with the workspace layout");
 constexpr int S_TOK_BOX = 128;                           // token rows per TMA box (per CTA)
 constexpr int S_W_BYTES = 2 * B_BOX_BYTES;               // 8 KB: 32 k-rows x 128 weight columns
 constexpr int S_T_BYTES = S_TOK_BOX * BK * 2;            // 8 KB: 128 token rows x 32 k (64-byte swizzle)
@@ -142,6 +143,7 @@ struct WinCoord {
   int j;      // 256-column weight tile
   int row0;   // first permuted row of the window
   int rows;   // real rows in the window (1..256)
+  int wid;    // window index over all experts (w_off[e] + window)
   bool ok;
 };
 
@@ -153,7 +155,7 @@ struct WinCoord {
 __device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const int32_t* s_win_off,
                                                   const int32_t* __restrict__ off_pad,
                                                   const int32_t* __restrict__ counts, int64_t max_rows) {
-  WinCoord c{0, 0, 0, 0, false};
+  WinCoord c{0, 0, 0, 0, 0, false};
   const int q = tile / NT;
   int lo = 0, hi = E;  // last e with s_win_off[e] <= q
   while (lo < hi) {
@@ -175,6 +177,7 @@ __device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const
   c.j = rem / gs;
   c.row0 = __ldg(off_pad + e) + S * w;
   c.rows = min(S, cnt - S * w);
+  c.wid = s_win_off[e] + w;
   // the window's rows lie inside the expert's padded range
   const int pad_end = __ldg(off_pad + e + 1);
   c.ok = c.rows > 0 && c.rows <= S_TOK && c.row0 >= 0 && c.row0 + c.rows <= pad_end && pad_end <= max_rows &&
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
                                const __grid_constant__ CUtensorMap tmW1, uint16_t* __restrict__ D,
                                const int32_t* __restrict__ off_pad, const int32_t* __restrict__ counts, int E,
                                int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status,
-                               uint32_t* __restrict__ sched) {
+                               uint32_t* __restrict__ sched, uint32_t* __restrict__ win_done, uint32_t win_target) {
   using C = SwapCfg<kUp>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,7 +270,13 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
-  pdl_launch_dependents();
+  // Per-window hand-off inside one forward (win_done set): the gate/up GEMM
+  // counts each window's finished tiles, and the down GEMM that follows it
+  // waits for its windows' counts instead of for the whole grid, so its
+  // clusters start on the SMs this grid frees.  This grid then lets it launch
+  // only after its own wait below (the rows and routing it reads are final).
+  const bool tracked = win_done != nullptr;
+  if (!(kUp && tracked)) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -295,7 +304,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     tmem_relinquish_pair();
   }
 
-  pdl_wait();
+  if (kUp || !tracked) pdl_wait();
+  if (kUp && tracked) pdl_launch_dependents();
   if (warp == 2) {
     // windows per expert (ceil(count / 256)) -> exclusive scan, E <= 256
     constexpr int per = MAX_E / 32;
@@ -367,6 +377,12 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         };
         const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
         if (!c.ok) record_status(status, kStatusBounds);
+        // down GEMM in a forward: this window's h rows are complete once all
+        // its gate/up tiles have counted in
+        if (!kUp && tracked && c.ok && !wait_counter_at_least(win_done + c.wid, win_target, abort_flag, status)) {
+          stop = true;
+          break;
+        }
         const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
         const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
         const int n0 = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank);  // first weight column
@@ -594,6 +610,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           }
         }
       }
+      if (kUp && tracked) {
+        // this warp's part of the window is written: count it (the warp's
+        // stores are ordered before the fence by the warp barrier)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(win_done + c.wid, 1u);
+        }
+      }
     }
   }
 
@@ -614,12 +639,17 @@ __global__ void __launch_bounds__(S_THREADS, 1)
 // untouched (the GEMM never stores their results).
 __global__ void scatter_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ scatter_idx,
                                     int64_t max_rows, int T, int H, int k, uint16_t* __restrict__ Xp,
-                                    uint32_t* __restrict__ status) {
+                                    uint32_t* __restrict__ win_done, int64_t n_win, uint32_t* __restrict__ status) {
   pdl_launch_dependents();
   pdl_wait();
+  // a forward's per-window counters start from zero (the previous forward's
+  // down GEMM, which read them, has completed)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = tid; win_done != nullptr && i < n_win; i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    win_done[i] = 0u;
   constexpr int CH = 1024;  // columns per work item: 16 bytes x 4 per lane
   const int lane = threadIdx.x & 31;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t warp0 = tid >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int nchunk = (H + CH - 1) / CH;
   const int64_t items = static_cast<int64_t>(T) * nchunk;
@@ -655,7 +685,8 @@ __global__ void scatter_rows_kernel(const uint16_t* __restrict__ X, const int32_
 
 template <bool kUp>
 cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, const int32_t* off_pad,
-                        const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms, cudaStream_t st) {
+                        const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
+                        int num_sms, cudaStream_t st) {
   using C = SwapCfg<kUp>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -672,9 +703,10 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
   // their stores are skipped
   const int NT = kUp ? (s.I + 255) / 256 : (s.H + C::TILE_COLS - 1) / C::TILE_COLS;
   const int K = kUp ? s.H : s.I;
-  const int64_t T_k = static_cast<int64_t>(s.T) * s.k;
-  const int64_t max_windows = T_k / S_TOK + (s.E < T_k ? s.E : T_k);  // sum_e ceil(c_e / 256)
-  const int64_t max_tiles = max_windows * NT;
+  const int64_t max_tiles = max_windows_of(s) * NT;
+  // a window's h rows are complete when every epilogue warp of both CTAs has
+  // counted each of its gate/up tiles
+  const uint32_t win_target = 2u * S_EPI_WARPS * static_cast<uint32_t>((s.I + 255) / 256);
   int64_t clusters = num_sms / 2;
   if (max_tiles < clusters) clusters = max_tiles;
   if (clusters <= 0) return cudaSuccess;
@@ -693,30 +725,31 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_window_kernel<kUp>, maps.a, maps.b0, maps.b1, D, off_pad, counts,
-                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status, sched);
+                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status, sched, win_done,
+                            win_target);
 }
 
 }  // namespace
 
 cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
-                                uint32_t* status, cudaStream_t st) {
+                                uint32_t* win_done, uint32_t* status, cudaStream_t st) {
   const int64_t items = static_cast<int64_t>(s.T) * ((s.H + 1023) / 1024);
   int64_t blocks = (items + 7) / 8;  // 8 warps (items) per CTA
   if (blocks > 4096) blocks = 4096;
   return launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, X, scatter_idx,
-                    max_rows_of(s), s.T, s.H, s.k, Xp, status);
+                    max_rows_of(s), s.T, s.H, s.k, Xp, win_done, max_windows_of(s), status);
 }
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
-                           const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
-                           cudaStream_t st) {
-  return launch_gemm<true>(s, maps, h, off_pad, counts, status, sched, num_sms, st);
+                           const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
+                           int num_sms, cudaStream_t st) {
+  return launch_gemm<true>(s, maps, h, off_pad, counts, status, sched, win_done, num_sms, st);
 }
 
 cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
-                             const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
-                             cudaStream_t st) {
-  return launch_gemm<false>(s, maps, Y, off_pad, counts, status, sched, num_sms, st);
+                             const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
+                             int num_sms, cudaStream_t st) {
+  return launch_gemm<false>(s, maps, Y, off_pad, counts, status, sched, win_done, num_sms, st);
 }
 
 }  // namespace moe

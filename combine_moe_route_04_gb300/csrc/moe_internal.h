@@ -24,6 +24,13 @@ inline int64_t max_blocks_of(const moe_shape& s) {
   return (R + (kRowBlock - 1) * touched) / kRowBlock;
 }
 inline int64_t max_rows_of(const moe_shape& s) { return kRowBlock * max_blocks_of(s); }
+// The GEMMs cut an expert's c rows into ceil(c / kWindowRows) token windows;
+// their number over all experts is at most T*k / kWindowRows + min(E, T*k).
+constexpr int kWindowRows = 256;
+inline int64_t max_windows_of(const moe_shape& s) {
+  const int64_t tk = static_cast<int64_t>(s.T) * s.k;
+  return tk / kWindowRows + (s.E < tk ? s.E : tk);
+}
 inline int64_t num_chunks_of(const moe_shape& s) { return (s.T + kChunkTokens - 1) / kChunkTokens; }
 
 // Byte offsets of everything the workspace holds.
@@ -34,6 +41,7 @@ struct WsLayout {
   size_t topk_ids, topk_w, counts, off_pad, block_expert, num_blocks, gather_idx, scatter_idx;
   size_t h;             // bf16 [max_rows][I]
   size_t y;             // bf16 [max_rows][H]
+  size_t win_done;      // uint32 [max_windows]: a forward's per-window gate/up tile counts
   size_t total;
 };
 WsLayout ws_layout(const moe_shape& s);
@@ -75,8 +83,9 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
                          uint32_t* status, cudaStream_t st);
 
 // Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token.
+// win_done (or nullptr): the forward's per-window counters, cleared here.
 cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
-                                uint32_t* status, cudaStream_t st);
+                                uint32_t* win_done, uint32_t* status, cudaStream_t st);
 
 struct GemmMaps {
   CUtensorMap a;     // token rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32
@@ -86,12 +95,15 @@ struct GemmMaps {
 
 // sched: the kernel's tile counter and its done counter (two uint32 in the
 // workspace's first 256 bytes, zero between launches)
+// win_done (max_windows_of(s) counters, or nullptr): within one forward the
+// gate/up GEMM counts each window's stored tiles there and the down GEMM that
+// follows waits per window instead of for the whole previous grid.
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,
-                           const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
-                           cudaStream_t st);
+                           const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
+                           int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t* Y, const int32_t* off_pad,
-                             const int32_t* counts, uint32_t* status, uint32_t* sched, int num_sms,
-                             cudaStream_t st);
+                             const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
+                             int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
                            const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);

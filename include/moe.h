@@ -210,7 +210,12 @@ moe_status moe_combine(const moe_shape *shape, const moe_bf16 *Y,
                        moe_bf16 *out, void *ws, moe_stream_t stream);
 
 /* Steps 1-5 on one stream with no host synchronisation in between; all
- * intermediates live in `ws` (see moe_workspace_views). */
+ * intermediates live in `ws` (see moe_workspace_views).  Unlike the step
+ * calls, which start each kernel after the previous one has completed, the
+ * down GEMM here starts on each expert's token window as soon as every
+ * gate/up tile of that window is stored (a per-window count kept in `ws`,
+ * cleared by the row gather of each forward), so it fills the SMs the gate/up
+ * GEMM frees.  The output is bit-identical to the step calls'. */
 moe_status moe_forward(const moe_shape *shape, const float *logits, const moe_bf16 *X,
                        const moe_bf16 *W_gate, const moe_bf16 *W_up,
                        const moe_bf16 *W_down, moe_bf16 *out, void *ws,
