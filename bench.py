@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -49,10 +50,16 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the GEMM kernel's code (comments and blank lines left out, so
+    that an edit of comments alone keeps the recorded counters valid)."""
     h = hashlib.sha256()
     for n in ("moe_gemm.cu", "moe_device.cuh"):
-        with open(os.path.join(ROOT, "combine_moe_route_04_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "combine_moe_route_04_gb300", "csrc", n), encoding="utf-8") as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode("utf-8") + b"\n")
     return h.hexdigest()[:16]
 
 

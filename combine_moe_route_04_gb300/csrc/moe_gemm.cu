@@ -40,14 +40,19 @@
 //     step into accumulators g | u, so SiLU(g)*u meets in one thread) and
 //     commits stages back to both producers and results to both epilogues;
 //   * warps 2-9 of each CTA drain the accumulator (thread = weight column;
-//     two warps per 32-lane TMEM quarter, each taking half of the window's
-//     tokens) into registers, release it on CTA 0's accumulator-empty
-//     barrier, and write their column down the window's output rows (in the
-//     up GEMM neighbouring lanes swap token halves and store two columns of
-//     one token each).  The two accumulators fill TMEM (one set).
-// Every wait on an mbarrier is bounded; on a timeout the kernel records it in
-// the status word, the roles stop, in-flight copies and MMAs are drained
-// (bounded) and TMEM is freed before exit.
+//     two warps per 32-lane TMEM quarter, taking its 32-token chunks in
+//     turn) into registers, release it on CTA 0's accumulator-empty barrier
+//     once their last TMEM load has landed, and write their column down the
+//     window's output rows (in the up GEMM neighbouring lanes swap token
+//     halves and store two columns of one token each).  The two accumulators
+//     fill TMEM (one set);
+//   * inside one forward the two GEMMs hand over per window: the gate/up
+//     epilogue counts each stored tile on its window's counter, and the down
+//     GEMM's producers wait for their window's count instead of for the whole
+//     gate/up grid (see the kernel's entry).
+// Every wait on an mbarrier or a counter is bounded; on a timeout the kernel
+// records it in the status word, the roles stop, in-flight copies and MMAs
+// are drained (bounded) and TMEM is freed before exit.
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -64,7 +69,7 @@ constexpr uint32_t ACC_COLS = 256;
 constexpr int MAX_E = 256;
 
 // Epilogue warps: two per 32-lane TMEM quarter (a warp may read only the
-// quarter warp_id % 4), each draining and storing half of the window's tokens.
+// quarter warp_id % 4), draining and storing alternate 32-token chunks.
 constexpr int S_EPI_WARPS = 8;
 constexpr int S_EPI_SPLIT = S_EPI_WARPS / 4;             // warps sharing a lane quarter
 
