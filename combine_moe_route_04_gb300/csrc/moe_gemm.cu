@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     // ------------------------------------------------------ TMA producer (both CTAs)
     if (elect_one_sync()) {
       const uint64_t pol_t = policy_evict_last();
-      const uint64_t pol_w = policy_evict_normal();
+      const uint64_t pol_wn = policy_evict_normal();
+      const uint64_t pol_wf = policy_evict_first();
       uint32_t it = 0;
       bool stop = false;
       // CTA 0 draws the pair's tiles and publishes them; CTA 1 reads them
@@ -388,6 +389,9 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           stop = true;
           break;
         }
+        // a one-window expert reads this weight tile once: evict it first and
+        // keep the rows, h and Y in L2; windows sharing a tile read it together
+        const uint64_t pol_w = (s_win_off[c.e + 1] - s_win_off[c.e]) == 1 ? pol_wf : pol_wn;
         const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
         const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
         const int n0 = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank);  // first weight column
