@@ -119,7 +119,8 @@ moe_status run_up_rows(const moe_shape& s, const uint16_t* Xp, const int32_t* co
   GemmMaps m;
   const uint64_t EH = static_cast<uint64_t>(s.E) * s.H;
   if (!encode_bf16_2d(&m.a, Xp, mr, s.H, 128, 32) || !encode_bf16_2d(&m.b0, Wg, EH, s.I, 32, 64) ||
-      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64))
+      !encode_bf16_2d(&m.b1, Wu, EH, s.I, 32, 64) || !encode_bf16_2d(&m.a64, Xp, mr, s.H, 64, 32) ||
+      !encode_bf16_2d(&m.a80, Xp, mr, s.H, 80, 32))
     return MOE_ERR_CUDA;
   return cuda_status(
       launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), win_done, num_sms, st));
@@ -140,7 +141,8 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts
   const uint64_t mr = static_cast<uint64_t>(max_rows_of(s));
   GemmMaps m;
   const uint64_t EI = static_cast<uint64_t>(s.E) * s.I;
-  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64))
+  if (!encode_bf16_2d(&m.a, h, mr, s.I, 128, 32) || !encode_bf16_2d(&m.b0, Wd, EI, s.H, 32, 64) ||
+      !encode_bf16_2d(&m.a64, h, mr, s.I, 64, 32) || !encode_bf16_2d(&m.a80, h, mr, s.I, 80, 32))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
   return cuda_status(

@@ -33,8 +33,9 @@
 //   * warp 0 of each CTA, TMA producer: per 32-deep K stage, its weight
 //     columns (two 32x64 boxes per accumulator, 128-byte swizzle: the up
 //     GEMM loads W_gate and W_up, the down GEMM two neighbouring blocks of
-//     W_down) and its token rows (128x32, 64-byte swizzle) into a ring of 9
-//     stages of 24 KB; all loads complete on CTA 0's full barriers;
+//     W_down) and its token rows (a 128x32 box, or 64 / 80 rows for a short
+//     window; 64-byte swizzle) into a ring of 9 stages of 24 KB; all loads
+//     complete on CTA 0's full barriers;
 //   * warp 1 allocates 512 TMEM columns in both CTAs; in CTA 0 one elected
 //     lane issues the MMAs (the up GEMM issues a W_gate and a W_up MMA per K
 //     step into accumulators g | u, so SiLU(g)*u meets in one thread) and
@@ -251,7 +252,8 @@ __device__ __forceinline__ int draw_tile(uint32_t* ctr, int total_tiles, int ncl
 
 template <bool kUp>
 __global__ void __launch_bounds__(S_THREADS, 1)
-    grouped_gemm_window_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmW0,
+    grouped_gemm_window_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmT64,
+                               const __grid_constant__ CUtensorMap tmT80, const __grid_constant__ CUtensorMap tmW0,
                                const __grid_constant__ CUtensorMap tmW1, uint16_t* __restrict__ D,
                                const int32_t* __restrict__ off_pad, const int32_t* __restrict__ counts, int E,
                                int K, int NT, int N_out, int64_t max_rows, uint32_t* __restrict__ status,
@@ -300,6 +302,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tmap(&tmT);
+    prefetch_tmap(&tmT64);
+    prefetch_tmap(&tmT80);
     prefetch_tmap(&tmW0);
     prefetch_tmap(&tmW1);
   }
@@ -395,6 +399,19 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         const int n_half = ((c.rows + 15) / 16) * 8;                   // tokens this CTA supplies
         const int trow = c.row0 + static_cast<int>(rank) * n_half;     // its first token row
         const int n0 = c.j * C::TILE_COLS + (C::TILE_COLS / 2) * static_cast<int>(rank);  // first weight column
+        // the token box: 128 rows, or 64 / 80 when this CTA supplies no more
+        // (short windows: fewer shared-memory bytes per stage; the MMA reads
+        // only the first n_half rows either way)
+        const CUtensorMap* tmap = &tmT;
+        int box_rows = S_TOK_BOX;
+        if (n_half <= 64) {
+          tmap = &tmT64;
+          box_rows = 64;
+        } else if (n_half <= 80) {
+          tmap = &tmT80;
+          box_rows = 80;
+        }
+        const uint32_t stage_tx = 2u * static_cast<uint32_t>(2 * S_W_BYTES + box_rows * BK * 2);
         for (int kb = 0; c.ok && kb < KB; ++kb, ++it) {
           if (!published && kb == KB / 2 && !publish()) {
             stop = true;
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             stop = true;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* st = sStage + s * C::STAGE_BYTES;
           const uint32_t fb = full0 + 8u * s;
           const int k0 = c.e * K + kb * BK;
@@ -419,7 +436,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             tma_load_2d_pair(st + S_W_BYTES, &tmW0, fb, n0 + 128, k0, pol_w);
             tma_load_2d_pair(st + S_W_BYTES + B_BOX_BYTES, &tmW0, fb, n0 + 192, k0, pol_w);
           }
-          tma_load_2d_pair(st + 2 * S_W_BYTES, &tmT, fb, kb * BK, trow, pol_t);
+          tma_load_2d_pair(st + 2 * S_W_BYTES, tmap, fb, kb * BK, trow, pol_t);
         }
         if (stop) break;
         if (!published && !publish()) break;
@@ -733,8 +750,8 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_window_kernel<kUp>, maps.a, maps.b0, maps.b1, D, off_pad, counts,
-                            s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status, sched, win_done,
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_window_kernel<kUp>, maps.a, maps.a64, maps.a80, maps.b0, maps.b1, D,
+                            off_pad, counts, s.E, K, NT, kUp ? s.I : s.H, max_rows_of(s), status, sched, win_done,
                             win_target);
 }
 

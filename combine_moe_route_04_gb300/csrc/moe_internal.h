@@ -91,6 +91,8 @@ struct GemmMaps {
   CUtensorMap a;     // token rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32
   CUtensorMap b0;    // weights, up: W_gate [E*H][I]; down: W_down [E*I][H]; box 32 x 64
   CUtensorMap b1;    // weights, up: W_up   [E*H][I]; down: unused (copy of b0)
+  CUtensorMap a64;   // the same token rows, box 64 x 32 (windows of <= 128 rows)
+  CUtensorMap a80;   // the same token rows, box 80 x 32 (windows of <= 160 rows)
 };
 
 // sched: the kernel's tile counter and its done counter (two uint32 in the
