@@ -112,7 +112,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, watts = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for _, ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -123,11 +123,16 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            try:
+                watts.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(watts) if watts else None}
 
 
 def dist_init():
@@ -395,9 +400,12 @@ def run_ours(args, world, rank, local):
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot b copied in
     ev_done = [torch.cuda.Event() for _ in range(2)]   # forward of slot b finished
     ev_out = [torch.cuda.Event() for _ in range(2)]    # output of slot b copied out
-    Ke = max(10, K // 4)
+    Ke = max(10, K)   # as many steps as the kernel-only loop: comparable time under the power cap
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_clocks = ClockSampler(local)
+    if rank == 0:
+        e2e_clocks.start()
     torch.cuda.synchronize(dev)
     e0.record(cs_in)
     cs_out.wait_event(e0)
@@ -425,6 +433,7 @@ def run_ours(args, world, rank, local):
     e1.record(cs_in)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / Ke
+    e2e_clk = e2e_clocks.stop() if rank == 0 else None
     if not torch.equal(out_h[(Ke - 1) & 1], out_d[(Ke - 1) & 1].cpu()):
         raise RuntimeError("end-to-end output copy mismatch")
     h2d = logits_h.numel() * 4 + x_h.numel() * 2
@@ -488,7 +497,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_cores, "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "clocks": e2e_clk},
         "gpu_launches": 7 * K,
         "clocks": clk,
     }
