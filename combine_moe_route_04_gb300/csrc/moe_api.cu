@@ -42,13 +42,15 @@ moe_status check_shape(const moe_shape* s) {
 moe_status prepare_device(cudaStream_t st, int* num_sms) {
   int dev = 0;
   cudaError_t err;
-  if (st != nullptr) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (st != nullptr && cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (st != nullptr && cs == cudaStreamCaptureStatusNone) {
     err = cudaStreamGetDevice(st, &dev);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
     if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
-  } else if (cudaGetDevice(&dev) != cudaSuccess) {
+  } else if (cudaGetDevice(&dev) != cudaSuccess) {  // no stream, or a stream being captured (its device is current)
     return MOE_ERR_CUDA;
   }
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;

@@ -31,6 +31,10 @@
  *     recorded in the workspace status word and reported by
  *     moe_last_device_status;
  *   - results are bitwise reproducible run to run (no floating-point atomics);
+ *   - the step calls and moe_forward may be recorded into a CUDA graph by
+ *     stream capture (they only launch kernels on `stream`; the launches keep
+ *     their programmatic-dependent-launch edges); moe_last_device_status
+ *     synchronises and is not capturable;
  *   - the device must have compute capability 10.3 (GB300), else MOE_ERR_ARCH.
  *
  * Supported shapes (else MOE_ERR_UNSUPPORTED_SHAPE): 1 <= T <= 2^22,
