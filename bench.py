@@ -4,11 +4,14 @@
 A step is one pass of the whole layer (route -> grouped gate/up GEMM with
 SiLU*up -> grouped down GEMM -> combine) over one batch of the pages-shaped
 workload (T=2048 tokens, H=4096, I=1536, E=64 experts, top-8), synthetic
-inputs already resident in HBM, timed as K calls of moe_forward (the
-library's one-call layer) between two CUDA events.  The metric is useful
+inputs already resident in HBM, timed as K replays of one moe_forward (the
+library's one-call layer) recorded into a CUDA graph, between two CUDA
+events (direct calls if capture is refused).  The metric is useful
 bf16 TFLOP/s (6*T*k*H*I FLOPs per step) with microseconds per layer beside
 it; a second pass through the four step calls, with events between them,
-gives the per-step breakdown and the up call's roofline.
+gives the per-step breakdown and the up call's roofline, and an end-to-end
+loop calls moe_forward on inputs copied in from host memory (and its output
+copied back) every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
