@@ -72,6 +72,8 @@ SMALL = {
     "k_equals_E": ((70, 256, 128, 4, 4), 80),
     "many_experts": ((96, 256, 128, 256, 16), 81),
     "smallest_dims": ((50, 128, 128, 3, 2), 82),      # H = I = 128: the down tile is half outside, K = 4 stages
+    "widest_hidden": ((8, 32768, 128, 2, 1), 83),     # H at its limit: 1024 K stages up, 64 down tiles per window
+    "widest_inner": ((40, 128, 32768, 3, 2), 84),     # I at its limit: 128 up tiles per window, 1024 K stages down
 }
 
 
