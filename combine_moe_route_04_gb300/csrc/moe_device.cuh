@@ -105,17 +105,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Waits until *ctr >= target, read with acquire at GPU scope, then orders
 // this thread's later async-proxy (TMA) reads of global memory after the
 // writes the counter published.  Gives up like mbar_wait, and also as soon as
-// the status word holds an error (the producer of the count may have stopped
-// on it; that error is the one reported).
+// the status word differs from `status_before` (an error raised since: the
+// producer of the count may have stopped on it; that error is the one
+// reported).
 __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint32_t target, volatile int* abort,
-                                                      uint32_t* status) {
+                                                      uint32_t* status, uint32_t status_before) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= target) break;
     if (*abort) return false;
-    if (status != nullptr && *reinterpret_cast<volatile uint32_t*>(status) != 0u) {
+    if (status != nullptr && *reinterpret_cast<volatile uint32_t*>(status) != status_before) {
       *abort = 1;
       return false;
     }

@@ -361,6 +361,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     // ------------------------------------------------------ TMA producer (both CTAs)
     if (elect_one_sync()) {
       const uint64_t pol_t = policy_evict_last();
+      // the status word when this forward began (written by its row gather)
+      const uint32_t status_before = (!kUp && tracked) ? __ldcg(status + kStatusSnapshotIndex) : 0u;
       const uint64_t pol_wn = policy_evict_normal();
       const uint64_t pol_wf = policy_evict_first();
       uint32_t it = 0;
@@ -389,7 +391,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         if (!c.ok) record_status(status, kStatusBounds);
         // down GEMM in a forward: this window's h rows are complete once all
         // its gate/up tiles have counted in
-        if (!kUp && tracked && c.ok && !wait_counter_at_least(win_done + c.wid, win_target, abort_flag, status)) {
+        if (!kUp && tracked && c.ok &&
+            !wait_counter_at_least(win_done + c.wid, win_target, abort_flag, status, status_before)) {
           stop = true;
           break;
         }
@@ -673,6 +676,10 @@ __global__ void scatter_rows_kernel(const uint16_t* __restrict__ X, const int32_
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t i = tid; win_done != nullptr && i < n_win; i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     win_done[i] = 0u;
+  // and the status word as this forward found it: the down GEMM's waits give
+  // up only on an error raised after this point
+  if (win_done != nullptr && tid == 0 && status != nullptr)
+    status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
   constexpr int CH = 1024;  // columns per work item: 16 bytes x 4 per lane
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = tid >> 5;

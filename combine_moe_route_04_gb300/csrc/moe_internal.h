@@ -57,6 +57,9 @@ inline uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 // moe_workspace_init clears (separate 64-byte lines)
 inline uint32_t* ws_sched_up(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 16; }
 inline uint32_t* ws_sched_down(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 32; }
+// the status word as a forward's row gather found it (see the down GEMM's
+// per-window wait), in the same cleared 256 bytes
+constexpr int kStatusSnapshotIndex = 48;
 
 // Launch with programmatic stream serialisation (the kernel must call
 // pdl_wait() before touching memory its predecessors use).

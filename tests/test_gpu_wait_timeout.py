@@ -48,3 +48,25 @@ def test_wait_check_rejects_bad_workspace():
     import combine_moe_route_04_gb300 as moe
     with pytest.raises(moe.MoEError):
         moe.check_wait_timeout(None)
+
+
+def test_unread_earlier_error_does_not_stop_a_forward(oracle_mod):
+    """The down GEMM's per-window waits give up only on an error raised during
+    the current forward: an earlier error nobody has read yet (here the
+    diagnostic's timeout) leaves the next forward exact, and is still the one
+    moe_last_device_status reports."""
+    torch = need_gpu()
+    import combine_moe_route_04_gb300 as moe
+    shape = (520, 256, 256, 16, 4)
+    s = moe.shape(*shape)
+    ws = moe.alloc_workspace(s)
+    moe.check_wait_timeout(ws)                   # sets the timeout bit; not read here
+    T, H, I, E, k = shape
+    logits = moe_inputs.make_logits(T, E, 98)
+    x = moe_inputs.make_tokens(T, H, 98)
+    wg, wu, wd = moe_inputs.make_weights(E, H, I, 98)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_forward(s, to_dev(logits), to_dev_bf16(x), to_dev_bf16(wg), to_dev_bf16(wu), to_dev_bf16(wd), out, ws)
+    assert moe.last_device_status(ws) == MOE_ERR_TIMEOUT
+    assert_close_layer(host_u16(out), oracle_mod.layer(logits, x, wg, wu, wd, k).out)
+    assert moe.last_device_status(ws) == 0
