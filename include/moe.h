@@ -91,11 +91,13 @@ moe_status moe_capacity(const moe_shape *shape, int64_t *max_blocks, int64_t *ma
  * of one shape; calls sharing it must be ordered on one stream. */
 moe_status moe_workspace_size(const moe_shape *shape, size_t *bytes);
 
-/* Clears the workspace status word and the gate/up GEMM's tile counter (all
- * in the first 256 bytes of `ws`).  Call once after allocating `ws`
- * (asynchronous, on `stream`); the GEMM leaves its counter cleared for the
- * next call.  On a workspace that was never cleared the gate/up GEMM may
- * skip tiles; it reports MOE_ERR_DEVICE_BOUNDS when a draw is out of range. */
+/* Clears the first 256 bytes of `ws`: the status word, both GEMMs' tile
+ * counters and the slot where each forward records the status it started
+ * with.  Call once after allocating `ws` (asynchronous, on `stream`); the
+ * GEMMs leave their counters cleared for the next call.  On a workspace that
+ * was never cleared a GEMM may skip tiles; it reports MOE_ERR_DEVICE_BOUNDS
+ * when a draw is out of range.  (The per-window counts of moe_forward, further
+ * on in `ws`, are cleared by every forward itself.) */
 moe_status moe_workspace_init(const moe_shape *shape, void *ws, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the error recorded by the kernels since the
