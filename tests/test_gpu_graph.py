@@ -1,4 +1,4 @@
-"""moe_forward captured into a CUDA graph (stream capture of its seven kernel
+"""moe_forward (and the step calls) captured into a CUDA graph (stream capture of its seven kernel
 launches, programmatic-dependent-launch edges included) and replayed: every
 replay equals a direct call on the same inputs bit for bit, also when new
 inputs are copied into the captured buffers between replays.  The pages-shaped
@@ -50,4 +50,50 @@ def test_graph_replay_equals_direct_calls(shape):
             g.replay()
             torch.cuda.synchronize()
             assert torch.equal(out, ref)
+    assert moe.last_device_status(ws) == 0
+
+
+def test_step_calls_captured_in_one_graph():
+    """The four step calls recorded into one graph (route -> up -> down ->
+    combine, each on buffers of the caller) replay to the same bits as the
+    same calls made directly."""
+    torch = need_gpu()
+    import combine_moe_route_04_gb300 as moe
+    shape = (520, 512, 384, 16, 4)
+    T, H, I, E, k = shape
+    s = moe.shape(*shape)
+    logits = to_dev(moe_inputs.make_logits(T, E, 45))
+    x = to_dev_bf16(moe_inputs.make_tokens(T, H, 45))
+    wg, wu, wd = (to_dev_bf16(w) for w in moe_inputs.make_weights(E, H, I, 45))
+    ws = moe.alloc_workspace(s)
+    r = moe.alloc_route_outputs(s)
+    mb, mr = moe.capacity(s)
+    h = torch.empty((mr, I), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((mr, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+
+    def steps():
+        moe.moe_route(s, logits, r["topk_ids"], r["topk_w"], r["counts"], r["off_pad"], r["block_expert"],
+                      r["num_blocks"], r["gather_idx"], r["scatter_idx"], ws)
+        moe.moe_grouped_gemm_up(s, x, r["scatter_idx"], r["counts"], r["off_pad"], wg, wu, h, ws)
+        moe.moe_grouped_gemm_down(s, h, r["counts"], r["off_pad"], wd, Y, ws)
+        moe.moe_combine(s, Y, r["scatter_idx"], r["topk_w"], out, ws)
+
+    steps()
+    torch.cuda.synchronize()
+    ref = out.clone()
+    assert moe.last_device_status(ws) == 0
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            steps()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out.zero_()
+        h.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
     assert moe.last_device_status(ws) == 0
