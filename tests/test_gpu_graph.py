@@ -1,8 +1,9 @@
-"""moe_forward (and the step calls) captured into a CUDA graph (stream capture of its seven kernel
-launches, programmatic-dependent-launch edges included) and replayed: every
-replay equals a direct call on the same inputs bit for bit, also when new
-inputs are copied into the captured buffers between replays.  The pages-shaped
-workload's per-window hand-off between the GEMMs runs inside the graph too."""
+"""CUDA graphs: moe_forward, and the four step calls, recorded by stream
+capture (the kernel launches with their programmatic-dependent-launch edges)
+and replayed.  Every replay equals the same calls made directly, bit for
+bit, also when new inputs are copied into the captured buffers between
+replays; the pages-shaped workload's per-window hand-off between the GEMMs
+runs inside the graph too."""
 import numpy as np
 import pytest
 
