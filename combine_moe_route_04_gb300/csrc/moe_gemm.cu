@@ -125,10 +125,12 @@ constexpr int S_TILE_READERS = 1 + S_EPI_WARPS + 1 + S_EPI_WARPS;
 // Both GEMMs run two 128-column accumulators per CTA that share each K
 // step's token rows: the up GEMM's gate and up columns, the down GEMM's two
 // neighbouring 128-column blocks (so a down tile is 512 weight columns, 256
-// per CTA).  A stage is 24 KB of loads for two MMAs, which keeps the
-// shared-memory traffic (TMA writes + MMA operand reads) below the data
-// path's bandwidth; the two accumulators fill TMEM, so there is one
-// accumulator set and the epilogue drain is not overlapped.
+// per CTA).  A stage is 24 KB of loads for two MMAs per 16-deep K substep:
+// the token rows, read by both tensor cores of the pair, serve two
+// accumulators, which is the least shared-memory traffic (TMA writes + MMA
+// operand reads) per FLOP that the MMA shape and TMEM allow.  The two
+// accumulators fill TMEM, so there is one accumulator set and the epilogue
+// drain is not overlapped.
 template <bool kUp>
 struct SwapCfg {
   static constexpr int TILE_COLS = kUp ? 256 : 512;      // output columns per tile
