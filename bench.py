@@ -167,6 +167,39 @@ def aggregate_tflops(world: int, flops_per_step: float, ms_per_step: float) -> f
     return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
+def layer_bytes(cfg, touched: int, r_pad: int) -> dict:
+    """Algorithmic bytes of each step of one layer: what the method must move
+    (useful rows only; every touched expert's weights once)."""
+    T, H, I, E, k = cfg.shape
+    R = T * k
+    return {"route": T * E * 4 + 12 * T * k + 4 * r_pad,
+            "up": touched * 2 * H * I * 2 + T * H * 2 + R * I * 2,
+            "down": touched * I * H * 2 + R * I * 2 + R * H * 2,
+            "combine": R * H * 2 + 8 * T * k + T * H * 2}
+
+
+def layer_roofline(cfg, touched: int, r_pad: int, ms_step: float, pk: dict, pk_src: str) -> dict:
+    """The layer's roofline: the slower of its useful FLOPs at the measured
+    sustained bf16 rate and its algorithmic bytes at the measured copy
+    bandwidth; frac = that floor / the measured time per layer."""
+    b = layer_bytes(cfg, touched, r_pad)
+    total_b = float(sum(b.values()))
+    flops = layer_flops(cfg)
+    t_hbm = total_b / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    t = ms_step * 1e-3
+    if t_hbm >= t_tc:
+        bound, achieved, peak, unit = "hbm", total_b / t / 1e9, pk["hbm_gbs"], "GB/s"
+        src = "%s hbm_gbs" % pk_src
+    else:
+        bound, achieved, peak, unit = "tensor", flops / t / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+        src = "%s bf16_tflops_sustained" % pk_src
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": max(t_hbm, t_tc) / t,
+            "peak_source": src, "floor_us": max(t_hbm, t_tc) * 1e6, "hbm_floor_us": t_hbm * 1e6,
+            "tensor_floor_us": t_tc * 1e6, "algorithmic_bytes": total_b, "bytes_by_step": b,
+            "useful_flops": flops, "us_per_layer": ms_step * 1e3}
+
+
 def cpu_oracle_sample(cfg, inp, seconds=15.0, max_tokens=256):
     """Times the oracle on the host cores on a bounded sample of the workload:
     routing for all tokens, then tokens' outputs one by one until ~`seconds`.
@@ -248,7 +281,10 @@ def run_reference(args, world, rank):
             "data": "synthetic", "impl": "reference",
             "config": {"workload": "%s (T=%d,H=%d,I=%d,E=%d,k=%d)" % ((cfg.name,) + cfg.shape)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "extrapolated": True},
+            "extrapolated": True,
+            "extrapolation": ("ms_per_step is an estimate of one whole layer on the host cores, scaled "
+                              "from each step's sample; the run itself takes a few tens of ms per step"),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -499,13 +535,18 @@ def run_ours(args, world, rank, local):
         return dict(extra, bound="tensor", achieved=tflops, peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
                     frac=tflops / pk["bf16_tflops_sustained"], peak_source="%s bf16_tflops_sustained" % pk_src)
 
-    # the GEMM kernel: each touched expert's W_gate and W_up once, each
-    # gathered row once, h written once
-    gemm_bytes = touched * 2 * H * I * 2 + T * k * H * 2 + T * k * I * 2
-    # the up call (gather + GEMM): each token row of X once instead
+    # Algorithmic bytes of the gate/up step (each touched expert's W_gate and
+    # W_up once, each token row of X once, h written once): the figure the
+    # kernel's roofline fraction is quoted on.  The kernel timed alone reads
+    # the gathered rows Xp (T*k rows) instead of X; that figure is reported
+    # beside it as frac_with_xp.
     up_bytes = touched * 2 * H * I * 2 + T * H * 2 + T * k * I * 2
-    roof = roofline_of(gemm_bytes, gemm_ms)
+    gemm_bytes_xp = touched * 2 * H * I * 2 + T * k * H * 2 + T * k * I * 2
+    roof = roofline_of(up_bytes, gemm_ms)
+    roof_xp = roofline_of(gemm_bytes_xp, gemm_ms)
     roof_call = roofline_of(up_bytes, up_ms)
+    nb = int(ws[v.num_blocks - ws.data_ptr():v.num_blocks - ws.data_ptr() + 4].view(torch.int32).item())
+    layer_roof = layer_roofline(cfg, touched, nb * 128, ms_step, pk, pk_src)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3,
@@ -521,9 +562,13 @@ def run_ours(args, world, rank, local):
         "step_by_step_us": steps_ms * 1e3,
         "roofline": dict(roof, kernel="grouped_gemm_window_kernel<up> (token-window CTA-pair tcgen05 grouped "
                                       "GEMM, timed through moe_grouped_gemm_up_rows)",
+                         bytes_model="touched experts' W_gate and W_up once + X once (T*H*2) + h once",
                          traffic=traffic,
+                         frac_with_xp=roof_xp["frac"],
+                         bytes_with_xp=gemm_bytes_xp,
                          up_call=dict(roof_call, kernel="moe_grouped_gemm_up call (row gather + the GEMM)",
                                       traffic=traffic_call)),
+        "layer_roofline": layer_roof,
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cpu_cores, "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

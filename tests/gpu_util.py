@@ -83,3 +83,33 @@ def ulp_dist_f32(a, b) -> np.ndarray:
     a = np.where(a < 0, -(a & 0x7FFFFFFF), a)
     b = np.where(b < 0, -(b & 0x7FFFFFFF), b)
     return np.abs(a - b)
+
+
+def assert_close_whole(got_bits, ref_bits, what, chunk_rows=4096):
+    """The layer tolerance over a whole 2-D array, in row chunks (bounded host
+    memory): every element within ATOL + RTOL*|ref|, the first bad rows
+    reported by index, and the relative Frobenius error over the WHOLE array
+    (accumulated across chunks) <= FRO.  Returns (max |err|, rel. Frobenius)."""
+    got_bits = np.asarray(got_bits)
+    ref_bits = np.asarray(ref_bits)
+    assert got_bits.shape == ref_bits.shape, "%s: shape %s vs %s" % (what, got_bits.shape, ref_bits.shape)
+    n = got_bits.shape[0]
+    d2 = 0.0
+    r2 = 0.0
+    max_err = 0.0
+    bad_rows = []
+    for r0 in range(0, n, chunk_rows):
+        g = f32(got_bits[r0:r0 + chunk_rows]).astype(np.float64)
+        r = f32(ref_bits[r0:r0 + chunk_rows]).astype(np.float64)
+        assert np.all(np.isfinite(g)), "%s: non-finite GPU values in rows %d.." % (what, r0)
+        err = np.abs(g - r)
+        bad = (err > ATOL + RTOL * np.abs(r)).any(axis=-1)
+        if bad.any() and len(bad_rows) < 16:
+            bad_rows.extend((r0 + np.nonzero(bad)[0][:16]).tolist())
+        max_err = max(max_err, float(err.max()) if err.size else 0.0)
+        d2 += float(np.sum((g - r) ** 2))
+        r2 += float(np.sum(r * r))
+    assert not bad_rows, "%s: rows %s out of tolerance (of %d), max err %g" % (what, bad_rows[:16], n, max_err)
+    fro = (d2 ** 0.5) / max(r2 ** 0.5, 1e-30)
+    assert fro <= FRO, "%s: relative Frobenius error %g > %g" % (what, fro, FRO)
+    return max_err, fro

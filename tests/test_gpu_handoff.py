@@ -80,3 +80,32 @@ def test_alternating_shapes_on_one_workspace():
             got = _forward(moe, s, d, ws)
             assert moe.last_device_status(ws) == 0
             assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("shape,bias", [((2048, 4096, 1536, 64, 8), "none"),
+                                        ((1024, 1024, 768, 16, 4), "zipf3")])
+def test_back_to_back_forwards_keep_counters_clean(shape, bias):
+    """Many forwards queued back to back on one stream, with no host
+    synchronisation between them: each forward's tile counters and per-window
+    counts must be back at zero before the next forward draws from them (a
+    counter left dirty would skip or repeat tiles and report
+    MOE_ERR_DEVICE_BOUNDS).  60 forwards in one burst, then 50 forwards each
+    followed by a status check; every output equals the step calls'."""
+    torch = need_gpu()
+    import combine_moe_route_04_gb300 as moe
+    s = moe.shape(*shape)
+    d = _inputs(shape, 73, bias)
+    ws = moe.alloc_workspace(s)
+    ref = _steps(moe, s, d, ws)
+    assert moe.last_device_status(ws) == 0
+    outs = [torch.empty((s.T, s.H), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    for i in range(60):
+        o = outs[i % 4]
+        moe.moe_forward(s, d["logits"], d["x"], d["wg"], d["wu"], d["wd"], o, ws)
+    assert moe.last_device_status(ws) == 0
+    for o in outs:
+        assert torch.equal(o, ref)
+    for i in range(50):
+        got = _forward(moe, s, d, ws)
+        assert moe.last_device_status(ws) == 0, "forward %d" % i
+        assert torch.equal(got, ref), "forward %d" % i

@@ -2,15 +2,19 @@
   * the tiny workload and small edge shapes against the full oracle layer;
   * the four full-size workloads (T=2048..16384, H=4096, I=1536, E=64/128,
     k=8): routing, counts, block table and permutation bit-exact over the whole
-    workload, and the outputs of sampled tokens (first, last, random, and
+    workload, and the WHOLE output, every real row of h and every real row of
+    Y against the full oracle layer, element by element, with the relative
+    Frobenius error taken over each whole tensor;
+  * the same workloads' outputs of sampled tokens (first, last, random, and
     tokens whose rows sit at the ragged end of an expert group) against the
-    oracle token by token, including their per-slot h and Y rows;
+    oracle token by token, including their per-slot h and Y rows (the
+    per-token path of the oracle, without its permutation);
   * determinism: two forwards give identical bits."""
 import numpy as np
 import pytest
 
 import moe_inputs
-from gpu_util import (assert_close_layer, assert_rows_close, host_u16, need_gpu, to_dev,
+from gpu_util import (assert_close_layer, assert_close_whole, assert_rows_close, host_u16, need_gpu, to_dev,
                       to_dev_bf16, ulp_dist_f32, W_ULPS)
 
 pytestmark = pytest.mark.gpu
@@ -144,6 +148,46 @@ def test_forward_full_workload_sampled(oracle_mod, n):
     # every output finite
     import torch
     assert bool(torch.isfinite(out.float()).all())
+
+
+def _whole_rows(ws, ptr, nrows, width):
+    import torch
+    off = ptr - ws.data_ptr()
+    return ws[off:off + nrows * width * 2].view(torch.int16).cpu().numpy().view(np.uint16).reshape(nrows, width)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n", [3, 2, 4, 5])
+def test_forward_full_workload_whole_output(oracle_mod, n):
+    """moe_forward on the full-size workload against the full oracle layer:
+    routing bit-exact, then the whole out [T, H], every real row of h and of Y,
+    each within the layer tolerance element by element and by relative
+    Frobenius error over the whole tensor."""
+    import combine_moe_route_04_gb300 as moe
+    cfg = moe_inputs.config(n)
+    inp = moe_inputs.make_inputs(cfg)
+    s, ws, dev, out = _forward(moe, cfg.shape, inp)
+    ref = oracle_mod.layer(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], cfg.k)
+    v = _view_arrays(moe, s, ws)
+    assert v["num_blocks"] == ref.route.num_blocks
+    assert np.array_equal(v["topk_ids"], ref.route.topk_ids)
+    assert np.array_equal(v["counts"], ref.route.counts)
+    assert np.array_equal(v["off_pad"], ref.route.off_pad)
+    assert np.array_equal(v["block_expert"], ref.route.block_expert)
+    assert np.array_equal(v["gather_idx"], ref.route.gather_idx)
+    assert np.array_equal(v["scatter_idx"], ref.route.scatter_idx)
+    assert ulp_dist_f32(v["topk_w"], ref.route.topk_w).max() <= W_ULPS
+    real = np.nonzero(ref.route.gather_idx >= 0)[0]
+    assert real.size == cfg.T * cfg.k
+    rows = ref.route.num_blocks * 128
+    h_got = _whole_rows(ws, v["h_ptr"], rows, cfg.I)[real]
+    assert_close_whole(h_got, ref.h[real], "h (every real row)")
+    del h_got
+    y_got = _whole_rows(ws, v["Y_ptr"], rows, cfg.H)[real]
+    assert_close_whole(y_got, ref.Y[real], "Y (every real row)")
+    del y_got
+    err, fro = assert_close_whole(host_u16(out), ref.out, "out (whole output)")
+    print("workload %d whole output: max |err| %.4g, relative Frobenius %.3g" % (n, err, fro))
 
 
 def test_forward_deterministic_and_reusable_workspace(oracle_mod):
