@@ -573,7 +573,7 @@ def run_ours(args, world, rank, local):
                          "sample": cpu_desc},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "clocks": e2e_clk},
-        "gpu_launches": 7 * K,
+        "gpu_launches": moe.FORWARD_KERNELS * K,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

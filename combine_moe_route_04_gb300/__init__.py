@@ -16,7 +16,7 @@ __all__ = ["MoEError", "MoEShape", "MoEViews", "lib_path", "load", "shape", "cap
            "workspace_size", "alloc_workspace", "workspace_init", "workspace_views",
            "last_device_status", "check_wait_timeout", "alloc_route_outputs", "moe_route",
            "moe_grouped_gemm_up", "moe_grouped_gemm_up_rows", "moe_grouped_gemm_down", "moe_combine",
-           "moe_forward", "STATUS_NAMES", "EXPORTS"]
+           "moe_forward", "STATUS_NAMES", "EXPORTS", "FORWARD_KERNELS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
@@ -24,6 +24,10 @@ _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS", 8: "MOE_ERR_SCRATCH_LIMIT"}
+
+# kernels one moe_forward launches: the routing's two, the row gather, the
+# gate/up and down GEMMs, the combine
+FORWARD_KERNELS = 6
 
 # every function include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_init",

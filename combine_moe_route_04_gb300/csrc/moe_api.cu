@@ -37,9 +37,10 @@ moe_status check_shape(const moe_shape* s) {
   return MOE_OK;
 }
 
-// Makes the stream's device current for this library and checks it is a
-// compute capability 10.3 part.
-moe_status prepare_device(cudaStream_t st, int* num_sms) {
+// Makes the stream's device current for this library's launches (the
+// previous current device goes into `restore`, which puts it back when the
+// entry point returns) and checks it is a compute capability 10.3 part.
+moe_status prepare_device(cudaStream_t st, int* num_sms, DeviceRestore* restore) {
   int dev = 0;
   cudaError_t err;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -49,7 +50,10 @@ moe_status prepare_device(cudaStream_t st, int* num_sms) {
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cur != dev) {
+      if (cudaSetDevice(dev) != cudaSuccess) return MOE_ERR_CUDA;
+      if (restore != nullptr && restore->prev < 0) restore->prev = cur;
+    }
   } else if (cudaGetDevice(&dev) != cudaSuccess) {  // no stream, or a stream being captured (its device is current)
     return MOE_ERR_CUDA;
   }
@@ -128,11 +132,13 @@ moe_status run_up_rows(const moe_shape& s, const uint16_t* Xp, const int32_t* co
       launch_gemm_up(s, m, h, off_pad, counts, w.status, ws_sched_up(w.status), win_done, num_sms, st));
 }
 
-// Row gather into the workspace's Xp, then the GEMM over it.
+// Row gather into the workspace's Xp (token by token: each row of X read
+// once), then the GEMM over it, which starts when the gather has completed.
+// win_done: nullptr, or the forward's per-window counters.
 moe_status run_up(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, const int32_t* counts,
                   const int32_t* off_pad, const uint16_t* Wg, const uint16_t* Wu,
                   uint16_t* h, const Views& w, uint32_t* win_done, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, win_done, w.status, st);
+  cudaError_t e = launch_scatter_rows(s, X, scatter_idx, w.xp, w.status, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return run_up_rows(s, w.xp, counts, off_pad, Wg, Wu, h, w, win_done, num_sms, st);
 }
@@ -153,7 +159,9 @@ moe_status run_down(const moe_shape& s, const uint16_t* h, const int32_t* counts
 
 }  // namespace
 
-moe_status device_ready(cudaStream_t st, int* num_sms) { return prepare_device(st, num_sms); }
+moe_status device_ready(cudaStream_t st, int* num_sms, DeviceRestore* restore) {
+  return prepare_device(st, num_sms, restore);
+}
 moe_status validate_shape(const moe_shape* s) { return check_shape(s); }
 
 WsLayout ws_layout(const moe_shape& s) {
@@ -181,7 +189,7 @@ WsLayout ws_layout(const moe_shape& s) {
   L.scatter_idx = take(T * k * 4);
   L.h = take(mr * static_cast<size_t>(s.I) * 2);
   L.y = take(mr * static_cast<size_t>(s.H) * 2);
-  L.win_done = take(static_cast<size_t>(max_windows_of(s)) * 4);
+  L.win_done = take(static_cast<size_t>(forward_counters_of(s)) * 4);
   L.total = off;
   return L;
 }
@@ -255,7 +263,8 @@ moe_status moe_workspace_init(const moe_shape* shape, void* ws, moe_stream_t str
   if (ws == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = prepare_device(s, nullptr);
+  DeviceRestore restore;
+  st = prepare_device(s, nullptr, &restore);
   if (st != MOE_OK) return st;
   return cuda_status(cudaMemsetAsync(ws, 0, 256, s));
 }
@@ -263,7 +272,8 @@ moe_status moe_workspace_init(const moe_shape* shape, void* ws, moe_stream_t str
 moe_status moe_last_device_status(void* ws, moe_stream_t stream) {
   if (ws == nullptr) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  moe_status st = prepare_device(s, nullptr);
+  DeviceRestore restore;
+  moe_status st = prepare_device(s, nullptr, &restore);
   if (st != MOE_OK) return st;
   uint32_t word = 0;
   if (cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -281,7 +291,8 @@ moe_status moe_check_wait_timeout(void* ws, moe_stream_t stream) {
   if (ws == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  moe_status st = prepare_device(s, nullptr);
+  DeviceRestore restore;
+  moe_status st = prepare_device(s, nullptr, &restore);
   if (st != MOE_OK) return st;
   return cuda_status(launch_wait_timeout(static_cast<uint32_t*>(ws), s));
 }
@@ -298,11 +309,13 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
     if (!aligned16(p)) return MOE_ERR_MISALIGNED;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = prepare_device(s, nullptr);
+  DeviceRestore restore;
+  st = prepare_device(s, nullptr, &restore);
   if (st != MOE_OK) return st;
   const Views w = views_of(*shape, ws);
   return cuda_status(launch_route(*shape, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
-                                  gather_idx, scatter_idx, w.chunk_counts, w.status, s));
+                                  gather_idx, scatter_idx, w.chunk_counts, ws_route_counter(w.status), nullptr, 0,
+                                  w.status, s));
 }
 
 moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const int32_t* scatter_idx,
@@ -317,7 +330,8 @@ moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const 
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int sms = 0;
-  st = prepare_device(s, &sms);
+  DeviceRestore restore;
+  st = prepare_device(s, &sms, &restore);
   if (st != MOE_OK) return st;
   return run_up(*shape, X, scatter_idx, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), nullptr, sms, s);
 }
@@ -334,7 +348,8 @@ moe_status moe_grouped_gemm_up_rows(const moe_shape* shape, const moe_bf16* Xp, 
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int sms = 0;
-  st = prepare_device(s, &sms);
+  DeviceRestore restore;
+  st = prepare_device(s, &sms, &restore);
   if (st != MOE_OK) return st;
   return run_up_rows(*shape, Xp, counts, off_pad, W_gate, W_up, h, views_of(*shape, ws), nullptr, sms, s);
 }
@@ -351,7 +366,8 @@ moe_status moe_grouped_gemm_down(const moe_shape* shape, const moe_bf16* h, cons
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int sms = 0;
-  st = prepare_device(s, &sms);
+  DeviceRestore restore;
+  st = prepare_device(s, &sms, &restore);
   if (st != MOE_OK) return st;
   return run_down(*shape, h, counts, off_pad, W_down, Y, views_of(*shape, ws), nullptr, sms, s);
 }
@@ -367,7 +383,8 @@ moe_status moe_combine(const moe_shape* shape, const moe_bf16* Y, const int32_t*
   }
   if (ws != nullptr && !aligned16(ws)) return MOE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = prepare_device(s, nullptr);
+  DeviceRestore restore;
+  st = prepare_device(s, nullptr, &restore);
   if (st != MOE_OK) return st;
   uint32_t* status = ws ? views_of(*shape, ws).status : nullptr;
   return cuda_status(launch_combine(*shape, Y, scatter_idx, topk_w, out, status, s));
@@ -384,13 +401,15 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int sms = 0;
-  st = prepare_device(s, &sms);
+  DeviceRestore restore;
+  st = prepare_device(s, &sms, &restore);
   if (st != MOE_OK) return st;
   const moe_shape& sh = *shape;
   const Views w = views_of(sh, ws);
   const moe_views& v = w.v;
   if (launch_route(sh, logits, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
-                   v.gather_idx, v.scatter_idx, w.chunk_counts, w.status, s) != cudaSuccess)
+                   v.gather_idx, v.scatter_idx, w.chunk_counts, ws_route_counter(w.status), w.win_done,
+                   forward_counters_of(sh), w.status, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   // the down GEMM starts on each token window as soon as its h rows are in
   st = run_up(sh, X, v.scatter_idx, v.counts, v.off_pad, W_gate, W_up, v.h, w, w.win_done, sms, s);

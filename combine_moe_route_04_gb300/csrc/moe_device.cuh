@@ -131,6 +131,13 @@ __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* ctr, uint3
   return true;
 }
 
+// Acquire-release fence at GPU scope.  Before a relaxed atomic it makes the
+// pair a release (this thread's earlier writes, and those ordered before them
+// by a barrier, are visible to whoever observes the atomic); after one, an
+// acquire.  Much cheaper than the sequentially consistent fence of
+// __threadfence() under heavy memory traffic.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel of the library starts with launch_dependents (the next kernel
 // may be scheduled once every CTA of this one has started) and calls wait

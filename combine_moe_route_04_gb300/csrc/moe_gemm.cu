@@ -55,6 +55,7 @@
 // records it in the status word, the roles stop, in-flight copies and MMAs
 // are drained (bounded) and TMEM is freed before exit.
 #include <cstdint>
+#include <mutex>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -283,7 +284,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   // counts each window's finished tiles, and the down GEMM that follows it
   // waits for its windows' counts instead of for the whole grid, so its
   // clusters start on the SMs this grid frees.  This grid then lets it launch
-  // only after its own wait below (the rows and routing it reads are final).
+  // only after its own wait below (the rows and routing it reads are final;
+  // the routing cleared the counts).
   const bool tracked = win_done != nullptr;
   if (!(kUp && tracked)) pdl_launch_dependents();
 
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     // ------------------------------------------------------ TMA producer (both CTAs)
     if (elect_one_sync()) {
       const uint64_t pol_t = policy_evict_last();
-      // the status word when this forward began (written by its row gather)
+      // the status word when this forward began (recorded by its routing)
       const uint32_t status_before = (!kUp && tracked) ? __ldcg(status + kStatusSnapshotIndex) : 0u;
       const uint64_t pol_wn = policy_evict_normal();
       const uint64_t pol_wf = policy_evict_first();
@@ -646,13 +648,20 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         // stores are ordered before the fence by the warp barrier)
         __syncwarp();
         if (lane == 0) {
-          __threadfence();
+          fence_acq_rel_gpu();  // release: the warp's stores before the count
           atomicAdd(win_done + c.wid, 1u);
         }
       }
     }
   }
 
+  // The down GEMM of a forward skipped griddepcontrol.wait at entry; it waits
+  // here, once its work is done, so that its completion implies that of the
+  // whole gate/up grid (including the last cluster's reset of the gate/up
+  // tile counter): every later kernel of the stream that waits on this grid
+  // then finds the gate/up GEMM finished too.  By now the gate/up grid has
+  // stored every window, so this wait is short.
+  if (!kUp && tracked) pdl_wait();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();
@@ -670,19 +679,11 @@ __global__ void __launch_bounds__(S_THREADS, 1)
 // untouched (the GEMM never stores their results).
 __global__ void scatter_rows_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ scatter_idx,
                                     int64_t max_rows, int T, int H, int k, uint16_t* __restrict__ Xp,
-                                    uint32_t* __restrict__ win_done, int64_t n_win, uint32_t* __restrict__ status) {
+                                    uint32_t* __restrict__ status) {
   pdl_launch_dependents();
   pdl_wait();
-  // a forward's per-window counters start from zero (the previous forward's
-  // down GEMM, which read them, has completed)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (int64_t i = tid; win_done != nullptr && i < n_win; i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    win_done[i] = 0u;
-  // and the status word as this forward found it: the down GEMM's waits give
-  // up only on an error raised after this point
-  if (win_done != nullptr && tid == 0 && status != nullptr)
-    status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
-  constexpr int CH = 1024;  // columns per work item: 16 bytes x 4 per lane
+  constexpr int CH = kGatherCols;  // columns per work item: 16 bytes x 4 per lane
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = tid >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -723,15 +724,20 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
                         const int32_t* counts, uint32_t* status, uint32_t* sched, uint32_t* win_done,
                         int num_sms, cudaStream_t st) {
   using C = SwapCfg<kUp>;
+  // the shared-memory opt-in, once per device (host threads may race here)
   static bool attr_done[64] = {};
+  static std::mutex attr_mu;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_window_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::ALLOC);
-    if (err != cudaSuccess) return err;
-    attr_done[dev] = true;
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (dev >= 64 || !attr_done[dev]) {
+      err = cudaFuncSetAttribute(grouped_gemm_window_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::ALLOC);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) attr_done[dev] = true;
+    }
   }
   // 256 (up) / 512 (down) weight columns per tile; a last tile that reaches
   // past I or H is partly outside: TMA zero-fills those weight columns and
@@ -767,12 +773,12 @@ cudaError_t launch_gemm(const moe_shape& s, const GemmMaps& maps, uint16_t* D, c
 }  // namespace
 
 cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
-                                uint32_t* win_done, uint32_t* status, cudaStream_t st) {
-  const int64_t items = static_cast<int64_t>(s.T) * ((s.H + 1023) / 1024);
+                                uint32_t* status, cudaStream_t st) {
+  const int64_t items = static_cast<int64_t>(s.T) * gather_pieces_of(s);
   int64_t blocks = (items + 7) / 8;  // 8 warps (items) per CTA
   if (blocks > 4096) blocks = 4096;
   return launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, X, scatter_idx,
-                    max_rows_of(s), s.T, s.H, s.k, Xp, win_done, max_windows_of(s), status);
+                    max_rows_of(s), s.T, s.H, s.k, Xp, status);
 }
 
 cudaError_t launch_gemm_up(const moe_shape& s, const GemmMaps& maps, uint16_t* h, const int32_t* off_pad,

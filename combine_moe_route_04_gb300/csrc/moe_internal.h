@@ -32,6 +32,12 @@ inline int64_t max_windows_of(const moe_shape& s) {
   return tk / kWindowRows + (s.E < tk ? s.E : tk);
 }
 inline int64_t num_chunks_of(const moe_shape& s) { return (s.T + kChunkTokens - 1) / kChunkTokens; }
+// The hand-off counters of one forward: the gate/up tiles stored per token
+// window.
+inline int64_t forward_counters_of(const moe_shape& s) { return max_windows_of(s); }
+// columns of X copied per work item of the row gathers
+constexpr int kGatherCols = 1024;
+inline int gather_pieces_of(const moe_shape& s) { return (s.H + kGatherCols - 1) / kGatherCols; }
 
 // Byte offsets of everything the workspace holds.
 struct WsLayout {
@@ -41,14 +47,27 @@ struct WsLayout {
   size_t topk_ids, topk_w, counts, off_pad, block_expert, num_blocks, gather_idx, scatter_idx;
   size_t h;             // bf16 [max_rows][I]
   size_t y;             // bf16 [max_rows][H]
-  size_t win_done;      // uint32 [max_windows]: a forward's per-window gate/up tile counts
+  size_t win_done;      // uint32 [forward_counters]: a forward's per-window gate/up tile counts
   size_t total;
 };
 WsLayout ws_layout(const moe_shape& s);
 
-// Makes the stream's device current and checks it (compute capability 10.3);
+// Puts the calling thread's previous current device back when an entry point
+// returns, if device_ready changed it.
+struct DeviceRestore {
+  int prev = -1;
+  DeviceRestore() = default;
+  DeviceRestore(const DeviceRestore&) = delete;
+  DeviceRestore& operator=(const DeviceRestore&) = delete;
+  ~DeviceRestore() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+// Makes the stream's device current for the launches that follow (recording
+// the previous one in `restore`) and checks it (compute capability 10.3);
 // fetches the tensor-map encoder on first use.
-moe_status device_ready(cudaStream_t st, int* num_sms);
+moe_status device_ready(cudaStream_t st, int* num_sms, DeviceRestore* restore);
 // The shape checks every entry point applies (MOE_OK or the error code).
 moe_status validate_shape(const moe_shape* s);
 
@@ -60,6 +79,9 @@ inline uint32_t* ws_sched_down(void* ws) { return reinterpret_cast<uint32_t*>(ws
 // the status word as a forward's row gather found it (see the down GEMM's
 // per-window wait), in the same cleared 256 bytes
 constexpr int kStatusSnapshotIndex = 48;
+// the routing's chunk counter (the CTA that brings it to the chunk count scans
+// the histograms and puts it back to zero), in the same cleared 256 bytes
+inline uint32_t* ws_route_counter(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 56; }
 
 // Launch with programmatic stream serialisation (the kernel must call
 // pdl_wait() before touching memory its predecessors use).
@@ -80,15 +102,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Launchers (asynchronous; return cudaGetLastError()).
+// route_counter: a uint32 that is zero between calls (the call leaves it so).
+// fwd_counters (or nullptr): inside moe_forward, the forward's n_fwd hand-off
+// counters, cleared by the routing's second kernel (which also records the
+// status word as the forward found it).
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
                          int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
                          int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
-                         uint32_t* status, cudaStream_t st);
+                         uint32_t* route_counter, uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status,
+                         cudaStream_t st);
 
-// Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token.
-// win_done (or nullptr): the forward's per-window counters, cleared here.
+// Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token (each row of
+// X read once).
 cudaError_t launch_scatter_rows(const moe_shape& s, const uint16_t* X, const int32_t* scatter_idx, uint16_t* Xp,
-                                uint32_t* win_done, uint32_t* status, cudaStream_t st);
+                                uint32_t* status, cudaStream_t st);
 
 struct GemmMaps {
   CUtensorMap a;     // token rows (K-major): Xp [max_rows][H] or h [max_rows][I]; box 128 x 32

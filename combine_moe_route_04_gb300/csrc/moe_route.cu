@@ -1,5 +1,5 @@
 // moe_route.cu -- routing, expert histogram, 128-row padded block table and
-// the gather/scatter permutation, in three small kernels.
+// the gather/scatter permutation, in two small kernels.
 //
 // What it computes ("通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §4, table
 // of data-flow patterns: "dispatch + GEMM" reorders the rows by the route;
@@ -20,10 +20,10 @@
 //      pick sets its token's bit in a per-expert 32-bit mask (shared-memory
 //      OR), so an entry's stable in-chunk rank is the popcount of its
 //      expert's mask below its token and the chunk's count the whole
-//      popcount.
-//   2. route_chunk_scan: one warp per expert scans its chunk histogram (the
-//      chunk bases) and writes the expert's row count.
-//   3. route_scatter: every CTA scans the padded counts (off_pad) in shared
+//      popcount.  Each CTA then counts its chunk in on a counter; the CTA
+//      that counts the last chunk in scans every expert's chunk histogram
+//      (the chunk bases) and writes the experts' row counts.
+//   2. route_scatter: every CTA scans the padded counts (off_pad) in shared
 //      memory; one thread per (t, j) writes row = off_pad[e] + chunk base +
 //      in-chunk rank to scatter_idx and gather_idx; the block table and the
 //      padding rows' -1 are spread over all threads.
@@ -69,17 +69,78 @@ __device__ __forceinline__ float key_logit(uint64_t key) {
 }
 __device__ __forceinline__ int key_expert(uint64_t key) { return 0xFFFF - static_cast<int>(key & 0xFFFFu); }
 
+// Exclusive scan across the warp of one value per lane; returns the lane's
+// exclusive prefix and sets `total` to the warp's sum.
+__device__ __forceinline__ int warp_exclusive_scan(int v, int lane, int& total) {
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
+
+// One warp: exclusive scans of the chunk histograms of experts ea and eb
+// (eb >= E: none) into chunk bases, in place, and their total row counts.
+// Both experts' loads are issued before either is scanned, and only the
+// 32-chunk batches that exist are scanned.  The histograms were written by
+// other CTAs, so they are read through L2 (__ldcg).
+__device__ __forceinline__ void scan_expert_pair(int ea, int eb, int E, int nch, int lane,
+                                                 int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts) {
+  constexpr int U = 4;  // 32-chunk batches per expert loaded before any is scanned
+  int32_t* ca = chunk_counts + static_cast<int64_t>(ea) * nch;
+  int32_t* cb = chunk_counts + static_cast<int64_t>(eb < E ? eb : ea) * nch;
+  const bool has_b = eb < E;
+  int run_a = 0, run_b = 0;
+  for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+    int va[U], vb[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u + lane;
+      va[u] = (c < nch) ? __ldcg(ca + c) : 0;
+      vb[u] = (has_b && c < nch) ? __ldcg(cb + c) : 0;
+    }
+    const int nb = min(U, (nch - c0 + 31) / 32);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (u < nb) {
+        const int c = c0 + 32 * u + lane;
+        int ta, tb;
+        const int xa = warp_exclusive_scan(va[u], lane, ta);
+        const int xb = warp_exclusive_scan(vb[u], lane, tb);
+        if (c < nch) {
+          ca[c] = run_a + xa;
+          if (has_b) cb[c] = run_b + xb;
+        }
+        run_a += ta;
+        run_b += tb;
+      }
+    }
+  }
+  if (lane == 0) {
+    counts[ea] = run_a;
+    if (has_b) counts[eb] = run_b;
+  }
+}
+
 // Kernel 1: one CTA per chunk of 32 tokens, one warp per token: the k best
 // experts (k rounds of a warp-wide max over the keys, the winner removed
 // each round; slot j = j-th round) and the renormalised weights; then the
 // chunk's expert histogram and each entry's stable in-chunk rank from the
-// per-expert token masks.
+// per-expert token masks.  The CTA that finishes the last chunk (the one
+// whose arrival on route_counter, zero at the start of the call, returns
+// nch - 1) then turns every expert's chunk histogram into chunk bases and
+// writes counts; route_scatter puts the counter back to zero.
 // EPL = logits per lane (E <= 32 * EPL).
 template <int EPL>
 __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
     const float* __restrict__ logits, int T, int E, int k, int nch, int32_t* __restrict__ topk_ids,
-    float* __restrict__ topk_w, int32_t* __restrict__ local_rank, int32_t* __restrict__ chunk_counts) {
+    float* __restrict__ topk_w, int32_t* __restrict__ local_rank, int32_t* __restrict__ chunk_counts,
+    int32_t* __restrict__ counts, uint32_t* __restrict__ route_counter, uint32_t* __restrict__ status) {
   __shared__ uint32_t s_mask[kMaxE];  // bit w: token w of the chunk picked expert e
+  __shared__ int s_last;
 
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
@@ -156,44 +217,25 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
     local_rank[static_cast<int64_t>(t0 + warp) * k + lane] = __popc(s_mask[my_e] & ((1u << warp) - 1u));
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     chunk_counts[static_cast<int64_t>(e) * nch + chunk] = __popc(s_mask[e]);
-}
 
-// Kernel 2: one warp per expert: exclusive scan of its chunk histogram (the
-// chunk bases, in place) and its total row count.
-__global__ void __launch_bounds__(256) route_chunk_scan_kernel(int E, int nch, int32_t* __restrict__ chunk_counts,
-                                                               int32_t* __restrict__ counts) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (e >= E) return;
-  int32_t* cc = chunk_counts + static_cast<int64_t>(e) * nch;
-  int running = 0;
-  constexpr int U = 8;  // 32-chunk batches loaded before any is scanned
-  for (int c0 = 0; c0 < nch; c0 += 32 * U) {
-    int v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + 32 * u + lane;
-      v[u] = (c < nch) ? cc[c] : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + 32 * u + lane;
-      int incl = v[u];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (c < nch) cc[c] = running + incl - v[u];
-      running += __shfl_sync(0xffffffffu, incl, 31);
-    }
+  // count this chunk in (its histogram made visible first); the CTA that
+  // counts the last one in scans all histograms.  A count past nch means the
+  // counter was not zero at the start (a workspace never cleared).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();  // release: the CTA's histogram (ordered by the barrier) before the arrival
+    const uint32_t ticket = atomicAdd(route_counter, 1u);
+    if (ticket >= static_cast<uint32_t>(nch)) record_status(status, kStatusBounds);
+    s_last = ticket == static_cast<uint32_t>(nch - 1) ? 1 : 0;
+    if (s_last) fence_acq_rel_gpu();  // acquire: every other CTA's histogram
   }
-  if (lane == 0) counts[e] = running;
+  __syncthreads();
+  if (!s_last) return;
+  constexpr int kWarps = kTopkThreads / 32;
+  for (int e = warp; e < E; e += 2 * kWarps) scan_expert_pair(e, e + kWarps, E, nch, lane, chunk_counts, counts);
 }
 
-// Kernel 3: every CTA forms off_pad (exclusive scan of the 128-padded counts)
+// Kernel 2: every CTA forms off_pad (exclusive scan of the 128-padded counts)
 // in shared memory, then one thread per (t, j) writes its permuted row; the
 // block table and the padding rows' -1 are spread over all threads.
 __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, int nch, int64_t max_blocks,
@@ -205,6 +247,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
                                                             int32_t* __restrict__ off_pad,
                                                             int32_t* __restrict__ block_expert,
                                                             int32_t* __restrict__ num_blocks,
+                                                            uint32_t* __restrict__ route_counter,
+                                                            uint32_t* __restrict__ fwd_counters, int64_t n_fwd,
                                                             uint32_t* __restrict__ status) {
   __shared__ int32_t s_off[kMaxE + 1];
   __shared__ int32_t s_cnt[kMaxE];
@@ -212,6 +256,18 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
   pdl_launch_dependents();
   pdl_wait();
   const int tid = threadIdx.x;
+  // kernel 1 has completed: its chunk counter goes back to zero for the next
+  // call (also after a call that found it dirty)
+  if (blockIdx.x == 0 && tid == 0) *route_counter = 0u;
+  // inside moe_forward: the forward's hand-off counters start from zero (the
+  // previous forward's kernels that used them have completed), and the status
+  // word is recorded as this forward found it (a hand-off wait gives up only
+  // on an error raised after this point)
+  if (fwd_counters != nullptr) {
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+    for (int64_t i = g; i < n_fwd; i += static_cast<int64_t>(gridDim.x) * blockDim.x) fwd_counters[i] = 0u;
+    if (g == 0 && status != nullptr) status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
+  }
   const int lane = tid & 31, warp = tid >> 5;
   // block-wide exclusive scan of padded counts (E <= 256 = blockDim.x)
   const int c = (tid < E) ? __ldg(counts + tid) : 0;
@@ -282,7 +338,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
                          int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
-                         int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts, uint32_t* status,
+                         int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
+                         uint32_t* route_counter, uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status,
                          cudaStream_t st) {
   const int nch = static_cast<int>(num_chunks_of(s));
   cudaError_t err;
@@ -292,9 +349,7 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
           : epl <= 4 ? route_topk_hist_kernel<4>
                      : route_topk_hist_kernel<8>;
   err = launch_pdl(k1, dim3(nch), dim3(kTopkThreads), 0, st, logits, s.T, s.E, s.k, nch, topk_ids, topk_w,
-                   scatter_idx, chunk_counts);
-  if (err != cudaSuccess) return err;
-  err = launch_pdl(route_chunk_scan_kernel, dim3((s.E + 7) / 8), dim3(256), 0, st, s.E, nch, chunk_counts, counts);
+                   scatter_idx, chunk_counts, counts, route_counter, status);
   if (err != cudaSuccess) return err;
   const int64_t n = static_cast<int64_t>(s.T) * s.k;
   const int64_t work = n > static_cast<int64_t>(s.E) * kRowBlock ? n : static_cast<int64_t>(s.E) * kRowBlock;
@@ -303,7 +358,7 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
   err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.E, s.k, nch,
                    static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
                    static_cast<const int32_t*>(counts), static_cast<const int32_t*>(chunk_counts), scatter_idx,
-                   gather_idx, off_pad, block_expert, num_blocks, status);
+                   gather_idx, off_pad, block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -322,8 +377,12 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
 namespace moe {
 namespace {
 
-constexpr int64_t kNoAllocScratchInts = int64_t(1) << 18;  // 1 MiB of int32
+constexpr int64_t kNoAllocHistInts = int64_t(1) << 18;  // 1 MiB of int32 chunk histograms
+constexpr int64_t kNoAllocHeadInts = 64;                  // 256 bytes ahead of them: the chunk counter
+constexpr int64_t kNoAllocScratchInts = kNoAllocHeadInts + kNoAllocHistInts;
 
+// [0]: the routing's chunk counter (zero when the module is loaded; every
+// call leaves it at zero); [64 ..): the per-chunk expert histograms.
 __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
 int32_t* g_route_scratch_addr[64] = {};
@@ -358,17 +417,21 @@ extern "C" moe_status moe_route_noalloc(const moe_shape* shape, const float* log
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_MISALIGNED;
   }
-  if (static_cast<int64_t>(shape->E) * num_chunks_of(*shape) > kNoAllocScratchInts) return MOE_ERR_SCRATCH_LIMIT;
+  if (static_cast<int64_t>(shape->E) * num_chunks_of(*shape) > kNoAllocHistInts) return MOE_ERR_SCRATCH_LIMIT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = device_ready(s, nullptr);  // makes the stream's device current
+  DeviceRestore restore;
+  st = device_ready(s, nullptr, &restore);  // the stream's device is current until this call returns
   if (st != MOE_OK) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   int32_t* scratch = route_scratch_on_device(dev);
   if (scratch == nullptr) return MOE_ERR_CUDA;
   // Every chunk-histogram entry the scan and scatter read is written by the
-  // first kernel of this call, so stale contents need no clearing.
+  // first kernel of this call, so stale histograms need no clearing; the
+  // chunk counter starts at zero (module load) and each call's second kernel
+  // puts it back to zero.
   const cudaError_t e = launch_route(*shape, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
-                                     gather_idx, scatter_idx, scratch, /*status=*/nullptr, s);
+                                     gather_idx, scatter_idx, scratch + kNoAllocHeadInts,
+                                     reinterpret_cast<uint32_t*>(scratch), nullptr, 0, /*status=*/nullptr, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -35,7 +35,9 @@
  *     stream capture (they only launch kernels on `stream`; the launches keep
  *     their programmatic-dependent-launch edges); moe_last_device_status
  *     synchronises and is not capturable;
- *   - the device must have compute capability 10.3 (GB300), else MOE_ERR_ARCH.
+ *   - the device must have compute capability 10.3 (GB300), else MOE_ERR_ARCH;
+ *   - a call makes the stream's device current for its launches and puts the
+ *     calling thread's previous current device back before it returns.
  *
  * Supported shapes (else MOE_ERR_UNSUPPORTED_SHAPE): 1 <= T <= 2^22,
  * 1 <= E <= 256, 1 <= k <= min(E, 16), 128 <= H <= 32768 and
@@ -91,12 +93,13 @@ moe_status moe_capacity(const moe_shape *shape, int64_t *max_blocks, int64_t *ma
  * of one shape; calls sharing it must be ordered on one stream. */
 moe_status moe_workspace_size(const moe_shape *shape, size_t *bytes);
 
-/* Clears the first 256 bytes of `ws`: the status word, both GEMMs' tile
- * counters and the slot where each forward records the status it started
- * with.  Call once after allocating `ws` (asynchronous, on `stream`); the
- * GEMMs leave their counters cleared for the next call.  On a workspace that
- * was never cleared a GEMM may skip tiles; it reports MOE_ERR_DEVICE_BOUNDS
- * when a draw is out of range.  (The per-window counts of moe_forward, further
+/* Clears the first 256 bytes of `ws`: the status word, the routing's chunk
+ * counter, both GEMMs' tile counters and the slot where each forward records
+ * the status it started with.  Call once after allocating `ws` (asynchronous,
+ * on `stream`); the kernels leave their counters cleared for the next call.
+ * On a workspace that was never cleared the routing may scan its histograms
+ * early and a GEMM may skip tiles; each reports MOE_ERR_DEVICE_BOUNDS when a
+ * counter is out of range, and the next call finds the counters cleared.  (The per-window counts of moe_forward, further
  * on in `ws`, are cleared by every forward itself.) */
 moe_status moe_workspace_init(const moe_shape *shape, void *ws, moe_stream_t stream);
 
@@ -115,6 +118,11 @@ moe_status moe_last_device_status(void *ws, moe_stream_t stream);
 moe_status moe_check_wait_timeout(void *ws, moe_stream_t stream);
 
 /* Steps 1-2: routing, histogram, padded block table and permutation.
+ * Passages: "通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §4, table row
+ * "dispatch + GEMM" (the routed rows are reordered by the route before the
+ * GEMM); "Lecture 11: Programming Systems for Specialized Hardware" example 4
+ * (softmax as exp -> sum -> divide); "通算融合算子（三）：ThunderKittens 多卡编程与
+ * 可融合的 GEMM 模板" §4 (128 rows = task block = expert alignment unit).
  *   logits       [T, E]  float32 (finite values)
  *   topk_ids     [T, k]  int32  out: picked experts, slot order
  *   topk_w       [T, k]  float32 out: renormalised weights
@@ -124,7 +132,8 @@ moe_status moe_check_wait_timeout(void *ws, moe_stream_t stream);
  *   num_blocks   [1]     int32  out: number of blocks (stays on the device)
  *   gather_idx   [max_rows] int32 out: token of each permuted row, -1 for padding
  *   scatter_idx  [T, k]  int32  out: permuted row of each (token, slot)
- *   ws           workspace (scratch: per-chunk expert histograms)
+ *   ws           workspace (scratch: per-chunk expert histograms; the chunk
+ *                counter in its cleared first 256 bytes)
  * Counts, table and permutation are exact; topk_ids are exact for the
  * float32 logits given; topk_w is within a few float32 ulps of the
  * correctly rounded value. */
@@ -143,16 +152,20 @@ moe_status moe_route(const moe_shape *shape, const float *logits,
  * or a deployment that reserves its memory up front and forbids allocation
  * once running (cudaMalloc may also synchronise the device and stall other
  * streams).  The pages describe no such variant; it has no counterpart there.
- *   - Limit: E * ceil(T/32) <= 262144 (1 MiB of int32 scratch; e.g. E=128
- *     with T up to 65536, E=256 with T up to 32768); larger shapes return
- *     MOE_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Limit: E * ceil(T/32) <= 262144 (1 MiB of int32 histograms, plus 256
+ *     bytes for a counter; e.g. E=128 with T up to 65536, E=256 with T up to
+ *     32768); larger shapes return MOE_ERR_SCRATCH_LIMIT and launch nothing.
  *   - The scratch is one array per device, shared by every call and held
  *     until the process exits.  Calls whose work may overlap on the GPU (on
  *     different streams without ordering) race on it; order them on one
- *     stream.  Every scratch entry a call reads is written earlier in the
- *     same call, so nothing needs clearing between calls.
+ *     stream.  Every histogram entry a call reads is written earlier in the
+ *     same call, and the one counter that must start at zero is zero when
+ *     the library is loaded and is put back to zero by every call, so
+ *     nothing needs clearing between calls.
  *   - The first call on a device looks up the scratch address on that device
- *     (a host-side query, no allocation) and caches it.
+ *     (a host-side query, no allocation) and caches it.  That lookup may load
+ *     the library's module on the device, so make the first call on each
+ *     device before capturing any stream into a CUDA graph.
  *   - Kernel-side errors are not reported (there is no status word).
  * Arguments as moe_route, without ws. */
 moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
@@ -162,6 +175,13 @@ moe_status moe_route_noalloc(const moe_shape *shape, const float *logits,
                              moe_stream_t stream);
 
 /* Step 3: grouped gate/up GEMM with the SiLU(gate)*up epilogue.
+ * Passages: "通算融合算子（三）：ThunderKittens 多卡编程与可融合的 GEMM 模板" §4
+ * (grouped GEMM: each expert's rows multiply that expert's weights, tasks in
+ * expert order); "通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §1 (gate/up
+ * GEMM followed by SiLU; fused here into the GEMM's epilogue).
+ * The GEMM finds each expert's rows from counts and off_pad (rows off_pad[e]
+ * .. off_pad[e] + counts[e]) instead of from the block table, and cuts them
+ * into windows of at most 256 rows; block_expert and num_blocks are not read.
  *   X          [T, H] bf16 tokens
  *   scatter_idx, counts, off_pad: moe_route's outputs; the call first copies
  *              X[t] to permuted row scatter_idx[t, j] of a workspace buffer
@@ -182,8 +202,9 @@ moe_status moe_grouped_gemm_up(const moe_shape *shape, const moe_bf16 *X,
                                moe_stream_t stream);
 
 /* Step 3 on rows already grouped by expert (for callers whose dispatch
- * delivers them that way): the same GEMM and epilogue as
- * moe_grouped_gemm_up, without the row gather.
+ * delivers them that way, as the expert-parallel dispatch of "通算融合算子（一）"
+ * §4 does): the same GEMM and epilogue as moe_grouped_gemm_up, without the
+ * row gather.
  *   Xp         [max_rows, H] bf16: row r holds the token of permuted row r
  *              (the rows of expert e from off_pad[e], counts[e] of them;
  *              padding rows are not read into any stored result)
@@ -195,6 +216,10 @@ moe_status moe_grouped_gemm_up_rows(const moe_shape *shape, const moe_bf16 *Xp,
                                     moe_bf16 *h, void *ws, moe_stream_t stream);
 
 /* Step 4: grouped down GEMM.
+ * Passages: "通算融合算子（三）：ThunderKittens 多卡编程与可融合的 GEMM 模板" §4 (the
+ * same grouped GEMM); "通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §1 (the
+ * down GEMM after SiLU).  Like the gate/up call it takes counts and off_pad in
+ * place of the block table.
  *   h      [max_rows, I] bf16 (permuted rows), counts / off_pad from moe_route,
  *   W_down [E, I, H] bf16
  *   Y      [max_rows, H] bf16 out: Y[r] = bf16(h[r] W_down[expert of r]) for
@@ -205,6 +230,8 @@ moe_status moe_grouped_gemm_down(const moe_shape *shape, const moe_bf16 *h,
                                  moe_stream_t stream);
 
 /* Step 5: top-k weighted combine back to token order, without atomics.
+ * Passage: "通算融合算子（一）：为什么要把通信写进 GEMM kernel 里" §4, table row
+ * "GEMM + combine" (the epilogue's top-k weighted reduction).
  *   out[t, c] = bf16(sum_{j<k} topk_w[t,j] * Y[scatter_idx[t,j], c])
  * with a float32 accumulator in slot order, each product and each sum rounded
  * to float32 (no fused multiply-add).
@@ -216,7 +243,10 @@ moe_status moe_combine(const moe_shape *shape, const moe_bf16 *Y,
                        moe_bf16 *out, void *ws, moe_stream_t stream);
 
 /* Steps 1-5 on one stream with no host synchronisation in between; all
- * intermediates live in `ws` (see moe_workspace_views).  Unlike the step
+ * intermediates live in `ws` (see moe_workspace_views).  Passages: those of
+ * the five steps above; the per-window hand-off below follows the gate /
+ * epilogue hooks of "通算融合算子（三）" §4 (a producer signals a counter per row
+ * block, a consumer waits on it) inside one GPU.  Unlike the step
  * calls, which start each kernel after the previous one has completed, the
  * down GEMM here starts on each expert's token window as soon as every
  * gate/up tile of that window is stored (a per-window count kept in `ws`,
