@@ -25,9 +25,9 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_S
                 3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_ARCH", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS", 8: "MOE_ERR_SCRATCH_LIMIT"}
 
-# kernels one moe_forward launches: the routing's two, the row gather, the
-# gate/up and down GEMMs, the combine
-FORWARD_KERNELS = 6
+# kernels one moe_forward launches: the routing kernel, the permutation with the
+# row gather, the gate/up and down GEMMs, the combine
+FORWARD_KERNELS = 5
 
 # every function include/moe.h declares
 EXPORTS = ["moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_init",

@@ -89,6 +89,7 @@ struct Views {
   int32_t* chunk_counts;
   uint16_t* xp;
   uint32_t* win_done;
+  int32_t* local_rank;
   moe_views v;
 };
 
@@ -100,6 +101,7 @@ Views views_of(const moe_shape& s, void* ws) {
   w.chunk_counts = reinterpret_cast<int32_t*>(b + L.chunk_counts);
   w.xp = reinterpret_cast<uint16_t*>(b + L.xp);
   w.win_done = reinterpret_cast<uint32_t*>(b + L.win_done);
+  w.local_rank = reinterpret_cast<int32_t*>(b + L.local_rank);
   w.v.Xp = reinterpret_cast<moe_bf16*>(w.xp);
   w.v.topk_ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
   w.v.topk_w = reinterpret_cast<float*>(b + L.topk_w);
@@ -187,6 +189,7 @@ WsLayout ws_layout(const moe_shape& s) {
   L.num_blocks = take(4);
   L.gather_idx = take(mr * 4);
   L.scatter_idx = take(T * k * 4);
+  L.local_rank = take(T * k * 4);
   L.h = take(mr * static_cast<size_t>(s.I) * 2);
   L.y = take(mr * static_cast<size_t>(s.H) * 2);
   L.win_done = take(static_cast<size_t>(forward_counters_of(s)) * 4);
@@ -314,8 +317,8 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t* topk_
   if (st != MOE_OK) return st;
   const Views w = views_of(*shape, ws);
   return cuda_status(launch_route(*shape, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
-                                  gather_idx, scatter_idx, w.chunk_counts, ws_route_counter(w.status), nullptr, 0,
-                                  w.status, s));
+                                  gather_idx, scatter_idx, w.chunk_counts, ws_route_counter(w.status), w.status,
+                                  s));
 }
 
 moe_status moe_grouped_gemm_up(const moe_shape* shape, const moe_bf16* X, const int32_t* scatter_idx,
@@ -407,12 +410,14 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   const moe_shape& sh = *shape;
   const Views w = views_of(sh, ws);
   const moe_views& v = w.v;
-  if (launch_route(sh, logits, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
-                   v.gather_idx, v.scatter_idx, w.chunk_counts, ws_route_counter(w.status), w.win_done,
-                   forward_counters_of(sh), w.status, s) != cudaSuccess)
+  // routing, then the permutation and the row gather in one kernel
+  if (launch_route_gather(sh, logits, X, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
+                          v.gather_idx, v.scatter_idx, w.local_rank, w.chunk_counts, w.xp,
+                          ws_route_counter(w.status), w.win_done, forward_counters_of(sh), w.status,
+                          s) != cudaSuccess)
     return MOE_ERR_CUDA;
   // the down GEMM starts on each token window as soon as its h rows are in
-  st = run_up(sh, X, v.scatter_idx, v.counts, v.off_pad, W_gate, W_up, v.h, w, w.win_done, sms, s);
+  st = run_up_rows(sh, w.xp, v.counts, v.off_pad, W_gate, W_up, v.h, w, w.win_done, sms, s);
   if (st != MOE_OK) return st;
   st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, w.win_done, sms, s);
   if (st != MOE_OK) return st;

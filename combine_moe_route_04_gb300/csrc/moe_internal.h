@@ -45,6 +45,7 @@ struct WsLayout {
   size_t chunk_counts;  // int32 [E][num_chunks]: per-chunk expert histogram, later chunk bases
   size_t xp;            // bf16 [max_rows][H]: gathered activation rows
   size_t topk_ids, topk_w, counts, off_pad, block_expert, num_blocks, gather_idx, scatter_idx;
+  size_t local_rank;    // int32 [T][k]: a forward's in-chunk ranks (routing -> permutation)
   size_t h;             // bf16 [max_rows][I]
   size_t y;             // bf16 [max_rows][H]
   size_t win_done;      // uint32 [forward_counters]: a forward's per-window gate/up tile counts
@@ -103,14 +104,21 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Launchers (asynchronous; return cudaGetLastError()).
 // route_counter: a uint32 that is zero between calls (the call leaves it so).
-// fwd_counters (or nullptr): inside moe_forward, the forward's n_fwd hand-off
-// counters, cleared by the routing's second kernel (which also records the
-// status word as the forward found it).
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
                          int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
                          int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
-                         uint32_t* route_counter, uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status,
-                         cudaStream_t st);
+                         uint32_t* route_counter, uint32_t* status, cudaStream_t st);
+
+// Inside moe_forward: the routing's first kernel, then one kernel that builds
+// the permutation and gathers the rows (Xp[scatter_idx[t, j]] = X[t], each row
+// of X read once).  local_rank: [T, k] int32 scratch.  fwd_counters: the
+// forward's n_fwd hand-off counters, cleared by the second kernel (which also
+// records the status word as the forward found it).
+cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const uint16_t* X, int32_t* topk_ids,
+                                float* topk_w, int32_t* counts, int32_t* off_pad, int32_t* block_expert,
+                                int32_t* num_blocks, int32_t* gather_idx, int32_t* scatter_idx,
+                                int32_t* local_rank, int32_t* chunk_counts, uint16_t* Xp, uint32_t* route_counter,
+                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, cudaStream_t st);
 
 // Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token (each row of
 // X read once).

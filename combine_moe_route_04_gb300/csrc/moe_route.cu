@@ -235,38 +235,33 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   for (int e = warp; e < E; e += 2 * kWarps) scan_expert_pair(e, e + kWarps, E, nch, lane, chunk_counts, counts);
 }
 
-// Kernel 2: every CTA forms off_pad (exclusive scan of the 128-padded counts)
-// in shared memory, then one thread per (t, j) writes its permuted row; the
-// block table and the padding rows' -1 are spread over all threads.
-__global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, int nch, int64_t max_blocks,
-                                                            const int32_t* __restrict__ topk_ids,
-                                                            const int32_t* __restrict__ counts,
-                                                            const int32_t* __restrict__ chunk_base,
-                                                            int32_t* __restrict__ scatter_idx,  // in: rank, out: row
-                                                            int32_t* __restrict__ gather_idx,
-                                                            int32_t* __restrict__ off_pad,
-                                                            int32_t* __restrict__ block_expert,
-                                                            int32_t* __restrict__ num_blocks,
-                                                            uint32_t* __restrict__ route_counter,
-                                                            uint32_t* __restrict__ fwd_counters, int64_t n_fwd,
-                                                            uint32_t* __restrict__ status) {
-  __shared__ int32_t s_off[kMaxE + 1];
-  __shared__ int32_t s_cnt[kMaxE];
-  __shared__ int32_t s_warp[8];
-  pdl_launch_dependents();
-  pdl_wait();
+// The part of the permutation every permute kernel shares, run by every CTA
+// (all threads): off_pad (exclusive scan of the 128-padded counts) into
+// shared memory; CTA 0 writes off_pad and num_blocks; the block table and
+// the padding rows' gather index -1 spread over all threads.  Also resets
+// the first kernel's chunk counter, and inside moe_forward clears the
+// forward's hand-off counters and records the status word the forward
+// started with.  Returns the number of 128-row blocks.
+__device__ __forceinline__ int permute_common(int E, int64_t max_blocks, const int32_t* __restrict__ counts,
+                                              int32_t* s_off, int32_t* s_cnt, int32_t* s_warp,
+                                              int32_t* __restrict__ gather_idx, int32_t* __restrict__ off_pad,
+                                              int32_t* __restrict__ block_expert, int32_t* __restrict__ num_blocks,
+                                              uint32_t* __restrict__ route_counter,
+                                              uint32_t* __restrict__ fwd_counters, int64_t n_fwd,
+                                              uint32_t* __restrict__ status) {
   const int tid = threadIdx.x;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   // kernel 1 has completed: its chunk counter goes back to zero for the next
   // call (also after a call that found it dirty)
-  if (blockIdx.x == 0 && tid == 0) *route_counter = 0u;
+  if (gtid == 0) *route_counter = 0u;
   // inside moe_forward: the forward's hand-off counters start from zero (the
   // previous forward's kernels that used them have completed), and the status
   // word is recorded as this forward found it (a hand-off wait gives up only
   // on an error raised after this point)
   if (fwd_counters != nullptr) {
-    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
-    for (int64_t i = g; i < n_fwd; i += static_cast<int64_t>(gridDim.x) * blockDim.x) fwd_counters[i] = 0u;
-    if (g == 0 && status != nullptr) status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
+    for (int64_t i = gtid; i < n_fwd; i += nthreads) fwd_counters[i] = 0u;
+    if (gtid == 0 && status != nullptr) status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
   }
   const int lane = tid & 31, warp = tid >> 5;
   // block-wide exclusive scan of padded counts (E <= 256 = blockDim.x)
@@ -289,32 +284,12 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 
   int nb = s_off[E] / kRowBlock;
   if (nb > max_blocks) {  // impossible for valid expert ids; keep every later index in range
-    if (tid == 0 && blockIdx.x == 0) record_status(status, kStatusBounds);
+    if (gtid == 0) record_status(status, kStatusBounds);
     nb = static_cast<int>(max_blocks);
   }
-  const int64_t max_rows = max_blocks * kRowBlock;
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (blockIdx.x == 0) {
     for (int e = tid; e <= E; e += blockDim.x) off_pad[e] = s_off[e];
     if (tid == 0) *num_blocks = nb;
-  }
-  // entries
-  for (int64_t i = gtid; i < static_cast<int64_t>(T) * k; i += nthreads) {
-    const int t = static_cast<int>(i / k);
-    const int e = topk_ids[i];
-    if (e < 0 || e >= E) {
-      record_status(status, kStatusBounds);
-      continue;
-    }
-    const int64_t row = static_cast<int64_t>(s_off[e]) +
-                        chunk_base[static_cast<int64_t>(e) * nch + t / kChunkTokens] + scatter_idx[i];
-    if (row < 0 || row >= max_rows) {
-      record_status(status, kStatusBounds);
-      continue;
-    }
-    scatter_idx[i] = static_cast<int32_t>(row);
-    gather_idx[row] = t;
   }
   // block table: the expert whose padded range holds row 128*b
   for (int64_t b = gtid; b < nb; b += nthreads) {
@@ -332,6 +307,150 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
     const int64_t row = static_cast<int64_t>(s_off[e]) + s_cnt[e] + (g % kRowBlock);
     if (row < s_off[e + 1] && row < static_cast<int64_t>(nb) * kRowBlock) gather_idx[row] = -1;
   }
+  return nb;
+}
+
+// The permuted row of entry (t, j) picking expert e: the expert's first
+// padded row + the rows of earlier chunks + the rank inside the chunk; -1
+// (and a recorded error) if out of range.
+__device__ __forceinline__ int64_t entry_row(int t, int e, int E, int nch, const int32_t* s_off,
+                                             const int32_t* __restrict__ chunk_base, int32_t rank, int64_t max_rows,
+                                             uint32_t* status) {
+  if (e < 0 || e >= E) {
+    record_status(status, kStatusBounds);
+    return -1;
+  }
+  const int64_t row = static_cast<int64_t>(s_off[e]) + __ldg(chunk_base + static_cast<int64_t>(e) * nch + t / kChunkTokens) +
+                      rank;
+  if (row < 0 || row >= max_rows) {
+    record_status(status, kStatusBounds);
+    return -1;
+  }
+  return row;
+}
+
+// Kernel 2 (the step call moe_route): the shared part, then one thread per
+// (t, j) writes its permuted row to scatter_idx (which held its in-chunk
+// rank) and gather_idx.
+__global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, int nch, int64_t max_blocks,
+                                                            const int32_t* __restrict__ topk_ids,
+                                                            const int32_t* __restrict__ counts,
+                                                            const int32_t* __restrict__ chunk_base,
+                                                            int32_t* __restrict__ scatter_idx,  // in: rank, out: row
+                                                            int32_t* __restrict__ gather_idx,
+                                                            int32_t* __restrict__ off_pad,
+                                                            int32_t* __restrict__ block_expert,
+                                                            int32_t* __restrict__ num_blocks,
+                                                            uint32_t* __restrict__ route_counter,
+                                                            uint32_t* __restrict__ status) {
+  __shared__ int32_t s_off[kMaxE + 1];
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_warp[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  permute_common(E, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad, block_expert, num_blocks,
+                 route_counter, nullptr, 0, status);
+  const int64_t max_rows = max_blocks * kRowBlock;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = gtid; i < static_cast<int64_t>(T) * k; i += nthreads) {
+    const int t = static_cast<int>(i / k);
+    const int64_t row = entry_row(t, topk_ids[i], E, nch, s_off, chunk_base, scatter_idx[i], max_rows, status);
+    if (row < 0) continue;
+    scatter_idx[i] = static_cast<int32_t>(row);
+    gather_idx[row] = t;
+  }
+}
+
+// Inside moe_forward, kernel 2 and the row gather in one: the shared part,
+// then one warp per (token, 1024 columns of X): lanes j < k find the rows of
+// the token's k entries (the first piece's warp writes scatter_idx and
+// gather_idx), and the warp copies that piece of X[t] to each of them, so
+// each row of X is read once.  The in-chunk ranks come in a separate buffer
+// (local_rank), so no warp overwrites what another still reads.
+__global__ void __launch_bounds__(256) permute_gather_kernel(int T, int H, int E, int k, int nch,
+                                                             int64_t max_blocks,
+                                                             const int32_t* __restrict__ topk_ids,
+                                                             const int32_t* __restrict__ local_rank,
+                                                             const int32_t* __restrict__ counts,
+                                                             const int32_t* __restrict__ chunk_base,
+                                                             const uint16_t* __restrict__ X,
+                                                             uint16_t* __restrict__ Xp,
+                                                             int32_t* __restrict__ scatter_idx,
+                                                             int32_t* __restrict__ gather_idx,
+                                                             int32_t* __restrict__ off_pad,
+                                                             int32_t* __restrict__ block_expert,
+                                                             int32_t* __restrict__ num_blocks,
+                                                             uint32_t* __restrict__ route_counter,
+                                                             uint32_t* __restrict__ fwd_counters, int64_t n_fwd,
+                                                             uint32_t* __restrict__ status) {
+  __shared__ int32_t s_off[kMaxE + 1];
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_warp[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  permute_common(E, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad, block_expert, num_blocks,
+                 route_counter, fwd_counters, n_fwd, status);
+  const int64_t max_rows = max_blocks * kRowBlock;
+  constexpr int CH = kGatherCols;  // columns per work item: 16 bytes x 4 per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int npiece = (H + CH - 1) / CH;
+  const int64_t items = static_cast<int64_t>(T) * npiece;
+  for (int64_t item = warp0; item < items; item += nwarps) {
+    const int t = static_cast<int>(item / npiece);
+    const int piece = static_cast<int>(item % npiece);
+    const int c0 = piece * CH;
+    int my_row = -1;  // lane j < k: row of (t, j)
+    if (lane < k) {
+      const int64_t i = static_cast<int64_t>(t) * k + lane;
+      const int64_t row = entry_row(t, __ldg(topk_ids + i), E, nch, s_off, chunk_base, __ldg(local_rank + i),
+                                    max_rows, status);
+      if (row >= 0) {
+        my_row = static_cast<int>(row);
+        if (piece == 0) {
+          scatter_idx[i] = my_row;
+          gather_idx[row] = t;
+        }
+      }
+    }
+    const int nv = min(CH, H - c0) / 8;  // 16-byte vectors in this piece (H % 128 == 0)
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(t) * H + c0);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = lane + 32 * u;
+      if (idx < nv) v[u] = __ldg(src + idx);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (row < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(row) * H + c0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = lane + 32 * u;
+        if (idx < nv) dst[idx] = v[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+namespace {
+
+cudaError_t launch_route_topk(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
+                              int32_t* local_rank, int32_t* chunk_counts, int32_t* counts, uint32_t* route_counter,
+                              uint32_t* status, cudaStream_t st) {
+  const int nch = static_cast<int>(num_chunks_of(s));
+  const int epl = (s.E + 31) / 32;
+  auto k1 = epl <= 1 ? route_topk_hist_kernel<1>
+          : epl <= 2 ? route_topk_hist_kernel<2>
+          : epl <= 4 ? route_topk_hist_kernel<4>
+                     : route_topk_hist_kernel<8>;
+  return launch_pdl(k1, dim3(nch), dim3(kTopkThreads), 0, st, logits, s.T, s.E, s.k, nch, topk_ids, topk_w,
+                    local_rank, chunk_counts, counts, route_counter, status);
 }
 
 }  // namespace
@@ -339,17 +458,12 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_ids, float* topk_w,
                          int32_t* counts, int32_t* off_pad, int32_t* block_expert, int32_t* num_blocks,
                          int32_t* gather_idx, int32_t* scatter_idx, int32_t* chunk_counts,
-                         uint32_t* route_counter, uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status,
-                         cudaStream_t st) {
+                         uint32_t* route_counter, uint32_t* status, cudaStream_t st) {
   const int nch = static_cast<int>(num_chunks_of(s));
-  cudaError_t err;
-  const int epl = (s.E + 31) / 32;
-  auto k1 = epl <= 1 ? route_topk_hist_kernel<1>
-          : epl <= 2 ? route_topk_hist_kernel<2>
-          : epl <= 4 ? route_topk_hist_kernel<4>
-                     : route_topk_hist_kernel<8>;
-  err = launch_pdl(k1, dim3(nch), dim3(kTopkThreads), 0, st, logits, s.T, s.E, s.k, nch, topk_ids, topk_w,
-                   scatter_idx, chunk_counts, counts, route_counter, status);
+  // kernel 1 leaves each entry's in-chunk rank in scatter_idx; kernel 2
+  // replaces it by the entry's row
+  cudaError_t err = launch_route_topk(s, logits, topk_ids, topk_w, scatter_idx, chunk_counts, counts,
+                                      route_counter, status, st);
   if (err != cudaSuccess) return err;
   const int64_t n = static_cast<int64_t>(s.T) * s.k;
   const int64_t work = n > static_cast<int64_t>(s.E) * kRowBlock ? n : static_cast<int64_t>(s.E) * kRowBlock;
@@ -358,7 +472,30 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
   err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.E, s.k, nch,
                    static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
                    static_cast<const int32_t*>(counts), static_cast<const int32_t*>(chunk_counts), scatter_idx,
-                   gather_idx, off_pad, block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
+                   gather_idx, off_pad, block_expert, num_blocks, route_counter, status);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const uint16_t* X, int32_t* topk_ids,
+                                float* topk_w, int32_t* counts, int32_t* off_pad, int32_t* block_expert,
+                                int32_t* num_blocks, int32_t* gather_idx, int32_t* scatter_idx,
+                                int32_t* local_rank, int32_t* chunk_counts, uint16_t* Xp, uint32_t* route_counter,
+                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, cudaStream_t st) {
+  const int nch = static_cast<int>(num_chunks_of(s));
+  cudaError_t err = launch_route_topk(s, logits, topk_ids, topk_w, local_rank, chunk_counts, counts,
+                                      route_counter, status, st);
+  if (err != cudaSuccess) return err;
+  const int64_t items = static_cast<int64_t>(s.T) * gather_pieces_of(s);
+  const int64_t tail = static_cast<int64_t>(s.E) * kRowBlock / 256;  // enough threads for the padding rows
+  int64_t blocks = (items + 7) / 8;  // 8 warps (items) per CTA
+  if (blocks < tail) blocks = tail;
+  if (blocks > 4096) blocks = 4096;
+  err = launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.H, s.E,
+                   s.k, nch, static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
+                   static_cast<const int32_t*>(local_rank), static_cast<const int32_t*>(counts),
+                   static_cast<const int32_t*>(chunk_counts), X, Xp, scatter_idx, gather_idx, off_pad,
+                   block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -432,6 +569,6 @@ extern "C" moe_status moe_route_noalloc(const moe_shape* shape, const float* log
   // puts it back to zero.
   const cudaError_t e = launch_route(*shape, logits, topk_ids, topk_w, counts, off_pad, block_expert, num_blocks,
                                      gather_idx, scatter_idx, scratch + kNoAllocHeadInts,
-                                     reinterpret_cast<uint32_t*>(scratch), nullptr, 0, /*status=*/nullptr, s);
+                                     reinterpret_cast<uint32_t*>(scratch), /*status=*/nullptr, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
