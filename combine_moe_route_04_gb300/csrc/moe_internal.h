@@ -81,7 +81,8 @@ inline uint32_t* ws_sched_down(void* ws) { return reinterpret_cast<uint32_t*>(ws
 // per-window wait), in the same cleared 256 bytes
 constexpr int kStatusSnapshotIndex = 48;
 // the routing's chunk counter (the CTA that brings it to the chunk count scans
-// the histograms and puts it back to zero), in the same cleared 256 bytes
+// the histograms; the next kernel puts it back to zero) and the mark that scan
+// leaves, two words in the same cleared 256 bytes
 inline uint32_t* ws_route_counter(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 56; }
 
 // Launch with programmatic stream serialisation (the kernel must call

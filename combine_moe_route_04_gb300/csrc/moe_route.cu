@@ -42,6 +42,11 @@ namespace {
 constexpr int kMaxE = 256;
 constexpr int kTopkThreads = 32 * kChunkTokens;              // one warp per token of the chunk
 
+// route_counter[0]: kernel 1's chunk arrivals (zero at the start of a call);
+// route_counter[1]: the mark kernel 1's scanning CTA leaves once the chunk
+// bases and counts are written (cleared at the start of every call).
+__host__ __device__ constexpr uint32_t scan_mark(int nch) { return 0x5CA40000u ^ static_cast<uint32_t>(nch); }
+
 // exp(v - m) for float32 v <= m: the difference is split exactly into
 // d_hi + d_lo (2Sum) and exp(d_hi + d_lo) ~= exp(d_hi) * (1 + d_lo), so the
 // result carries expf's error only, not the rounding of v - m (which grows
@@ -152,6 +157,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
   __syncthreads();
   pdl_wait();  // inputs and outputs may be in use by the previous kernel until here
+  // no scan has happened in this call yet (thread 0 of CTA 0 clears the mark
+  // before its own arrival, so before the scanning CTA can set it)
+  if (chunk == 0 && threadIdx.x == 0) route_counter[1] = 0u;
 
   int my_e = 0;
   if (warp < ntok) {
@@ -233,6 +241,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   if (!s_last) return;
   constexpr int kWarps = kTopkThreads / 32;
   for (int e = warp; e < E; e += 2 * kWarps) scan_expert_pair(e, e + kWarps, E, nch, lane, chunk_counts, counts);
+  // the bases and counts are written: the next kernel may use them
+  if (threadIdx.x == 0) route_counter[1] = scan_mark(nch);
 }
 
 // The part of the permutation every permute kernel shares, run by every CTA
@@ -241,8 +251,13 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
 // the padding rows' gather index -1 spread over all threads.  Also resets
 // the first kernel's chunk counter, and inside moe_forward clears the
 // forward's hand-off counters and records the status word the forward
-// started with.  Returns the number of 128-row blocks.
-__device__ __forceinline__ int permute_common(int E, int64_t max_blocks, const int32_t* __restrict__ counts,
+// started with.  If kernel 1 left no scan mark (its counter was not zero at
+// the start, so no CTA scanned), counts are not this call's: the call
+// reports MOE_ERR_DEVICE_BOUNDS and routes every expert empty (CTA 0 writes
+// zero counts), so nothing is indexed from stale values.  Returns the number
+// of 128-row blocks.
+__device__ __forceinline__ int permute_common(int E, int nch, int64_t max_count, int64_t max_blocks,
+                                              int32_t* __restrict__ counts,
                                               int32_t* s_off, int32_t* s_cnt, int32_t* s_warp,
                                               int32_t* __restrict__ gather_idx, int32_t* __restrict__ off_pad,
                                               int32_t* __restrict__ block_expert, int32_t* __restrict__ num_blocks,
@@ -264,9 +279,19 @@ __device__ __forceinline__ int permute_common(int E, int64_t max_blocks, const i
     if (gtid == 0 && status != nullptr) status[kStatusSnapshotIndex] = *reinterpret_cast<volatile uint32_t*>(status);
   }
   const int lane = tid & 31, warp = tid >> 5;
+  const bool scanned = __ldcg(route_counter + 1) == scan_mark(nch);
+  if (!scanned && gtid == 0) record_status(status, kStatusBounds);
   // block-wide exclusive scan of padded counts (E <= 256 = blockDim.x)
-  const int c = (tid < E) ? __ldg(counts + tid) : 0;
+  int c = 0;
+  if (tid < E && scanned) {
+    c = __ldcg(counts + tid);
+    if (c < 0 || c > max_count) {  // impossible for a count this call scanned
+      record_status(status, kStatusBounds);
+      c = 0;
+    }
+  }
   if (tid < E) s_cnt[tid] = c;
+  if (!scanned && blockIdx.x == 0 && tid < E) counts[tid] = 0;
   const int padded = (c + kRowBlock - 1) / kRowBlock * kRowBlock;
   int incl = padded;
 #pragma unroll
@@ -305,7 +330,7 @@ __device__ __forceinline__ int permute_common(int E, int64_t max_blocks, const i
   for (int64_t g = gtid; g < static_cast<int64_t>(E) * kRowBlock; g += nthreads) {
     const int e = static_cast<int>(g / kRowBlock);
     const int64_t row = static_cast<int64_t>(s_off[e]) + s_cnt[e] + (g % kRowBlock);
-    if (row < s_off[e + 1] && row < static_cast<int64_t>(nb) * kRowBlock) gather_idx[row] = -1;
+    if (row >= 0 && row < s_off[e + 1] && row < static_cast<int64_t>(nb) * kRowBlock) gather_idx[row] = -1;
   }
   return nb;
 }
@@ -334,7 +359,7 @@ __device__ __forceinline__ int64_t entry_row(int t, int e, int E, int nch, const
 // rank) and gather_idx.
 __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k, int nch, int64_t max_blocks,
                                                             const int32_t* __restrict__ topk_ids,
-                                                            const int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ counts,
                                                             const int32_t* __restrict__ chunk_base,
                                                             int32_t* __restrict__ scatter_idx,  // in: rank, out: row
                                                             int32_t* __restrict__ gather_idx,
@@ -348,8 +373,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
   __shared__ int32_t s_warp[8];
   pdl_launch_dependents();
   pdl_wait();
-  permute_common(E, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad, block_expert, num_blocks,
-                 route_counter, nullptr, 0, status);
+  permute_common(E, nch, static_cast<int64_t>(T) * k, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad,
+                 block_expert, num_blocks, route_counter, nullptr, 0, status);
   const int64_t max_rows = max_blocks * kRowBlock;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -372,7 +397,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(int T, int H, int E
                                                              int64_t max_blocks,
                                                              const int32_t* __restrict__ topk_ids,
                                                              const int32_t* __restrict__ local_rank,
-                                                             const int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ counts,
                                                              const int32_t* __restrict__ chunk_base,
                                                              const uint16_t* __restrict__ X,
                                                              uint16_t* __restrict__ Xp,
@@ -389,8 +414,8 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(int T, int H, int E
   __shared__ int32_t s_warp[8];
   pdl_launch_dependents();
   pdl_wait();
-  permute_common(E, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad, block_expert, num_blocks,
-                 route_counter, fwd_counters, n_fwd, status);
+  permute_common(E, nch, static_cast<int64_t>(T) * k, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad,
+                 block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
   const int64_t max_rows = max_blocks * kRowBlock;
   constexpr int CH = kGatherCols;  // columns per work item: 16 bytes x 4 per lane
   const int lane = threadIdx.x & 31;
@@ -471,7 +496,7 @@ cudaError_t launch_route(const moe_shape& s, const float* logits, int32_t* topk_
   if (blocks > 1184) blocks = 1184;
   err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.E, s.k, nch,
                    static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
-                   static_cast<const int32_t*>(counts), static_cast<const int32_t*>(chunk_counts), scatter_idx,
+                   counts, static_cast<const int32_t*>(chunk_counts), scatter_idx,
                    gather_idx, off_pad, block_expert, num_blocks, route_counter, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
@@ -493,7 +518,7 @@ cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const u
   if (blocks > 4096) blocks = 4096;
   err = launch_pdl(permute_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s.T, s.H, s.E,
                    s.k, nch, static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
-                   static_cast<const int32_t*>(local_rank), static_cast<const int32_t*>(counts),
+                   static_cast<const int32_t*>(local_rank), counts,
                    static_cast<const int32_t*>(chunk_counts), X, Xp, scatter_idx, gather_idx, off_pad,
                    block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
   if (err != cudaSuccess) return err;
@@ -515,11 +540,12 @@ namespace moe {
 namespace {
 
 constexpr int64_t kNoAllocHistInts = int64_t(1) << 18;  // 1 MiB of int32 chunk histograms
-constexpr int64_t kNoAllocHeadInts = 64;                  // 256 bytes ahead of them: the chunk counter
+constexpr int64_t kNoAllocHeadInts = 64;                  // 256 bytes ahead of them: the counter words
 constexpr int64_t kNoAllocScratchInts = kNoAllocHeadInts + kNoAllocHistInts;
 
 // [0]: the routing's chunk counter (zero when the module is loaded; every
-// call leaves it at zero); [64 ..): the per-chunk expert histograms.
+// call leaves it at zero), [1]: the mark its scan leaves (cleared at the start
+// of every call); [64 ..): the per-chunk expert histograms.
 __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
 int32_t* g_route_scratch_addr[64] = {};

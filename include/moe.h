@@ -94,8 +94,8 @@ moe_status moe_capacity(const moe_shape *shape, int64_t *max_blocks, int64_t *ma
 moe_status moe_workspace_size(const moe_shape *shape, size_t *bytes);
 
 /* Clears the first 256 bytes of `ws`: the status word, the routing's chunk
- * counter, both GEMMs' tile counters and the slot where each forward records
- * the status it started with.  Call once after allocating `ws` (asynchronous,
+ * counter and scan mark, both GEMMs' tile counters and the slot where each
+ * forward records the status it started with.  Call once after allocating `ws` (asynchronous,
  * on `stream`); the kernels leave their counters cleared for the next call.
  * On a workspace that was never cleared the routing may scan its histograms
  * early and a GEMM may skip tiles; each reports MOE_ERR_DEVICE_BOUNDS when a
@@ -153,15 +153,16 @@ moe_status moe_route(const moe_shape *shape, const float *logits,
  * once running (cudaMalloc may also synchronise the device and stall other
  * streams).  The pages describe no such variant; it has no counterpart there.
  *   - Limit: E * ceil(T/32) <= 262144 (1 MiB of int32 histograms, plus 256
- *     bytes for a counter; e.g. E=128 with T up to 65536, E=256 with T up to
+ *     bytes for two counter words; e.g. E=128 with T up to 65536, E=256 with T up to
  *     32768); larger shapes return MOE_ERR_SCRATCH_LIMIT and launch nothing.
  *   - The scratch is one array per device, shared by every call and held
  *     until the process exits.  Calls whose work may overlap on the GPU (on
  *     different streams without ordering) race on it; order them on one
  *     stream.  Every histogram entry a call reads is written earlier in the
- *     same call, and the one counter that must start at zero is zero when
- *     the library is loaded and is put back to zero by every call, so
- *     nothing needs clearing between calls.
+ *     same call, and the counter that must start at zero is zero when the
+ *     library is loaded and is put back to zero by every call (the scan
+ *     mark beside it is cleared at the start of every call), so nothing
+ *     needs clearing between calls.
  *   - The first call on a device looks up the scratch address on that device
  *     (a host-side query, no allocation) and caches it.  That lookup may load
  *     the library's module on the device, so make the first call on each
