@@ -142,7 +142,9 @@ struct SwapCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1 + 2 * S_TILE_RING;
   static constexpr int WIN_OFF = BAR_OFF + NUM_BARS * 8 + 16;
   static constexpr int TILE_OFF = (WIN_OFF + (MAX_E + 1) * 4 + 15) / 16 * 16;
-  static constexpr int BYTES = TILE_OFF + S_TILE_RING * 4;
+  static constexpr int CNT_OFF = TILE_OFF + S_TILE_RING * 4;     // counts[e], copied at entry
+  static constexpr int OFFP_OFF = CNT_OFF + MAX_E * 4;           // off_pad[e], copied at entry
+  static constexpr int BYTES = OFFP_OFF + (MAX_E + 1) * 4;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(ALLOC <= 232448, "shared memory budget (window kernel)");
 };
@@ -162,8 +164,7 @@ struct WinCoord {
 // Tile t: expert e (windows w_off[e] .. w_off[e+1]), then groups of
 // S_GROUP_WINDOWS windows, then weight tile, then the window in the group.
 __device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const int32_t* s_win_off,
-                                                  const int32_t* __restrict__ off_pad,
-                                                  const int32_t* __restrict__ counts, int64_t max_rows) {
+                                                  const int32_t* s_offp, const int32_t* s_cnt, int64_t max_rows) {
   WinCoord c{0, 0, 0, 0, 0, false};
   const int q = tile / NT;
   int lo = 0, hi = E;  // last e with s_win_off[e] <= q
@@ -180,23 +181,25 @@ __device__ __forceinline__ WinCoord decode_window(int tile, int NT, int E, const
   const int rem = local - g * NT * S_GROUP_WINDOWS;
   const int gs = min(S_GROUP_WINDOWS, nw - g * S_GROUP_WINDOWS);
   const int w = g * S_GROUP_WINDOWS + rem % gs;
-  const int cnt = __ldg(counts + e);
+  const int cnt = s_cnt[e];
   const int S = ((cnt + nw - 1) / nw + 15) / 16 * 16;
   c.e = e;
   c.j = rem / gs;
-  c.row0 = __ldg(off_pad + e) + S * w;
+  c.row0 = s_offp[e] + S * w;
   c.rows = min(S, cnt - S * w);
   c.wid = s_win_off[e] + w;
   // the window's rows lie inside the expert's padded range
-  const int pad_end = __ldg(off_pad + e + 1);
+  const int pad_end = s_offp[e + 1];
   c.ok = c.rows > 0 && c.rows <= S_TOK && c.row0 >= 0 && c.row0 + c.rows <= pad_end && pad_end <= max_rows &&
          c.j < NT;
   return c;
 }
 
-// Dynamic tile scheduler.  CTA 0's producer lane draws tile indices from a
-// counter in global memory (atomicAdd, in tile order, so the windows that
-// share a weight tile are still drawn together) and publishes each into a
+// Dynamic tile scheduler.  Cluster c starts on tile c; after that CTA 0's
+// producer lane draws tile indices from a counter in global memory (tile
+// nclusters + the counter's old value, atomicAdd, in tile order, so the
+// windows that share a weight tile are still drawn together) and publishes
+// each into a
 // ring in both CTAs' shared memory; every other role of the pair reads the
 // same sequence from its own CTA's ring.  A cluster draws and publishes its
 // next tile when it starts the current one, so the index is in place a whole
@@ -242,17 +245,6 @@ __device__ __forceinline__ bool ring_put(const TileRing& r, uint32_t n, int tile
   return true;
 }
 
-// Draws the next tile index; a value past every possible draw means the
-// counter was not cleared (moe_workspace_init) and ends the sequence.
-__device__ __forceinline__ int draw_tile(uint32_t* ctr, int total_tiles, int nclusters, uint32_t* status) {
-  const uint32_t t = atomicAdd(ctr, 1u);
-  if (t >= static_cast<uint32_t>(total_tiles + nclusters)) {
-    record_status(status, kStatusBounds);
-    return total_tiles;
-  }
-  return static_cast<int>(t);
-}
-
 template <bool kUp>
 __global__ void __launch_bounds__(S_THREADS, 1)
     grouped_gemm_window_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmT64,
@@ -276,6 +268,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_win_off = reinterpret_cast<int32_t*>(smem + C::WIN_OFF);
+  int32_t* s_cnt = reinterpret_cast<int32_t*>(smem + C::CNT_OFF);
+  int32_t* s_offp = reinterpret_cast<int32_t*>(smem + C::OFFP_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -330,6 +324,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       int nw = 0;
       if (e < E) {
         const int cnt = __ldg(counts + e);
+        s_cnt[e] = cnt;  // the tile decoder's copy
         nw = cnt > 0 ? (cnt + S_TOK - 1) / S_TOK : 0;
       }
       loc[i] = nw;
@@ -349,6 +344,9 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       run += loc[i];
     }
     if (lane == 31 && 32 * per == E) s_win_off[E] = incl;
+  } else if (warp == 3) {
+    // the tile decoder's copy of the padded offsets
+    for (int e = lane; e <= E; e += 32) s_offp[e] = __ldg(off_pad + e);
   }
   tc_fence_before();
   __syncthreads();
@@ -371,27 +369,33 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       const uint64_t pol_wf = policy_evict_first();
       uint32_t it = 0;
       bool stop = false;
-      // CTA 0 draws the pair's tiles and publishes them; CTA 1 reads them
+      // each cluster's first tile is its cluster index (no draw in front of
+      // its first loads); CTA 0 draws the pair's later tiles and publishes
+      // them; CTA 1 reads them
       int tile;
       if (rank == 0) {
-        tile = draw_tile(sched, total_tiles, nclusters, status);
+        tile = static_cast<int>(blockIdx.x >> 1);
         stop = !ring_put(ring, 0, tile, abort_flag, status);
       } else {
         tile = ring_take(ring, 0, rank, rempty0, true, abort_flag, status);
       }
       for (uint32_t n = 0; !stop && tile >= 0 && tile < total_tiles; ++n) {
         // CTA 0 draws the next tile now without waiting for the value, and
-        // publishes it halfway through this tile's loads
+        // publishes it halfway through this tile's loads.  Draws follow the
+        // nclusters first tiles, one per tile processed, so a cleared counter
+        // yields nclusters .. total_tiles + nclusters - 1; a larger value
+        // means the counter was not cleared and ends the sequence.
         const uint32_t raw_next = rank == 0 ? atomicAdd(sched, 1u) : 0u;
         int next = total_tiles;
         bool published = rank != 0;
         auto publish = [&]() {
-          next = raw_next < static_cast<uint32_t>(total_tiles + nclusters) ? static_cast<int>(raw_next) : total_tiles;
-          if (next != static_cast<int>(raw_next)) record_status(status, kStatusBounds);
+          const uint64_t t = static_cast<uint64_t>(nclusters) + raw_next;
+          next = t < static_cast<uint64_t>(total_tiles + nclusters) ? static_cast<int>(t) : total_tiles;
+          if (static_cast<uint64_t>(next) != t) record_status(status, kStatusBounds);
           published = true;
           return ring_put(ring, n + 1, next, abort_flag, status);
         };
-        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+        const WinCoord c = decode_window(tile, NT, E, s_win_off, s_offp, s_cnt, max_rows);
         if (!c.ok) record_status(status, kStatusBounds);
         // down GEMM in a forward: this window's h rows are complete once all
         // its gate/up tiles have counted in
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       for (uint32_t n = 0; !stop; ++n) {
         const int tile = ring_take(ring, n, rank, rempty0, true, abort_flag, status);
         if (tile < 0 || tile >= total_tiles) break;
-        const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+        const WinCoord c = decode_window(tile, NT, E, s_win_off, s_offp, s_cnt, max_rows);
         if (!c.ok) continue;
         const uint32_t N = static_cast<uint32_t>(((c.rows + 15) / 16) * 16);
         const uint32_t idesc = idesc_base | ((N >> 3) << 17);
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       if (lane == 0) ring_release(ring, n, rank, rempty0);
       if (vote_any_epi(tile < 0)) break;
       if (tile >= total_tiles) break;
-      const WinCoord c = decode_window(tile, NT, E, s_win_off, off_pad, counts, max_rows);
+      const WinCoord c = decode_window(tile, NT, E, s_win_off, s_offp, s_cnt, max_rows);
       if (!c.ok) continue;
       const uint32_t a = 0;
       const uint32_t aph = tcount & 1u;
