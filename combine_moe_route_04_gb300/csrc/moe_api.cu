@@ -386,11 +386,12 @@ moe_status moe_combine(const moe_shape* shape, const moe_bf16* Y, const int32_t*
   }
   if (ws != nullptr && !aligned16(ws)) return MOE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int sms = 0;
   DeviceRestore restore;
-  st = prepare_device(s, nullptr, &restore);
+  st = prepare_device(s, &sms, &restore);
   if (st != MOE_OK) return st;
   uint32_t* status = ws ? views_of(*shape, ws).status : nullptr;
-  return cuda_status(launch_combine(*shape, Y, scatter_idx, topk_w, out, status, s));
+  return cuda_status(launch_combine(*shape, Y, scatter_idx, topk_w, out, status, sms, s));
 }
 
 moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf16* X, const moe_bf16* W_gate,
@@ -421,7 +422,7 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   if (st != MOE_OK) return st;
   st = run_down(sh, v.h, v.counts, v.off_pad, W_down, v.Y, w, w.win_done, sms, s);
   if (st != MOE_OK) return st;
-  return cuda_status(launch_combine(sh, v.Y, v.scatter_idx, v.topk_w, out, w.status, s));
+  return cuda_status(launch_combine(sh, v.Y, v.scatter_idx, v.topk_w, out, w.status, sms, s));
 }
 
 }  // extern "C"

@@ -6,8 +6,11 @@
 // with a float32 accumulator in slot order, each product and each sum rounded
 // to float32 (__fmul_rn / __fadd_rn keep the compiler from fusing them).
 //
-// One warp per token: a warp reads 512 contiguous bytes of each of the k
-// expert rows per load instruction and writes 512 contiguous bytes of out.
+// One warp per token, or per piece of a token when there are fewer tokens
+// than resident warps (decode): a warp reads 512 contiguous bytes of each of
+// the k expert rows per load instruction and writes 512 contiguous bytes of
+// out.  (Measured: pieces for every shape cost the large workloads 1.5%; one
+// warp per token left decode's 64 tokens on 8 SMs, 13 us slower.)
 // No atomics: results are bitwise reproducible.
 #include <cstdint>
 
@@ -17,15 +20,16 @@
 namespace moe {
 namespace {
 
-// One warp per token (grid-stride): lanes j < k load the token's row index and
-// weight once and broadcast them; then each lane gathers CH 16-byte chunks of
-// all k expert rows per iteration (k*CH loads in flight per lane) and sums
+// One warp per work item (grid-stride), an item being one of a token's ppt
+// pieces (ppt = 1: the whole token): lanes j < k load the token's row index
+// and weight and broadcast them; then per iteration each lane gathers CH
+// 16-byte chunks of all k expert rows (k*CH loads in flight per lane) and sums
 // them in slot order.
 template <int KMAX, int CH>
 __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restrict__ Y,
                                                       const int32_t* __restrict__ scatter_idx,
                                                       const float* __restrict__ topk_w, int T, int H, int k,
-                                                      int64_t max_rows, uint16_t* __restrict__ out,
+                                                      int64_t max_rows, int ppt, uint16_t* __restrict__ out,
                                                       uint32_t* __restrict__ status) {
   pdl_launch_dependents();
   pdl_wait();
@@ -33,7 +37,13 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int vpr = H / 8;  // 16-byte chunks per row
-  for (int64_t t = warp0; t < T; t += nwarps) {
+  const int iters = (vpr + 32 * CH - 1) / (32 * CH);  // iterations per row
+  const int per = (iters + ppt - 1) / ppt;              // iterations per piece
+  const int64_t items = static_cast<int64_t>(T) * ppt;
+  for (int64_t item = warp0; item < items; item += nwarps) {
+    const int64_t t = item / ppt;
+    const int first = static_cast<int>(item % ppt) * per * 32 * CH;
+    const int last = min(vpr, first + per * 32 * CH);
     int my_row = -1;
     float my_w = 0.0f;
     if (lane < k) {
@@ -41,7 +51,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
       my_w = __ldg(topk_w + t * k + lane);
       if (r >= 0 && r < max_rows) {
         my_row = static_cast<int>(r);
-      } else if (status != nullptr) {
+      } else if (status != nullptr && first == 0) {
         record_status(status, kStatusBounds);
       }
     }
@@ -54,7 +64,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
     }
     const uint4* Y4 = reinterpret_cast<const uint4*>(Y);
     uint4* orow = reinterpret_cast<uint4*>(out + t * H);
-    for (int c0 = 0; c0 < vpr; c0 += 32 * CH) {
+    for (int c0 = first; c0 < last; c0 += 32 * CH) {
       uint4 y[KMAX][CH];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
@@ -98,15 +108,22 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx, const float* topk_w,
-                           uint16_t* out, uint32_t* status, cudaStream_t st) {
-  int64_t blocks = (static_cast<int64_t>(s.T) + 7) / 8;  // 8 warps (tokens) per CTA
+                           uint16_t* out, uint32_t* status, int num_sms, cudaStream_t st) {
+  // pieces per token: as many as make the items fill the resident warps
+  // (2 CTAs of 8 warps per SM), at most one per iteration of the row
+  const int64_t vpr = s.H / 8;
+  const int64_t iters = s.k <= 8 ? (vpr + 63) / 64 : (vpr + 31) / 32;
+  int64_t ppt = static_cast<int64_t>(num_sms) * 16 / s.T;
+  if (ppt < 1) ppt = 1;
+  if (ppt > iters) ppt = iters;
+  int64_t blocks = (static_cast<int64_t>(s.T) * ppt + 7) / 8;  // 8 warps (items) per CTA
   if (blocks > 4096) blocks = 4096;
   const int64_t mr = max_rows_of(s);
   if (s.k <= 8)
     return launch_pdl(combine_kernel<8, 2>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, Y, scatter_idx,
-                      topk_w, s.T, s.H, s.k, mr, out, status);
+                      topk_w, s.T, s.H, s.k, mr, static_cast<int>(ppt), out, status);
   return launch_pdl(combine_kernel<16, 1>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, Y, scatter_idx,
-                    topk_w, s.T, s.H, s.k, mr, out, status);
+                    topk_w, s.T, s.H, s.k, mr, static_cast<int>(ppt), out, status);
 }
 
 }  // namespace moe

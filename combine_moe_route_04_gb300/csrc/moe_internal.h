@@ -147,7 +147,7 @@ cudaError_t launch_gemm_down(const moe_shape& s, const GemmMaps& maps, uint16_t*
                              int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx,
-                           const float* topk_w, uint16_t* out, uint32_t* status, cudaStream_t st);
+                           const float* topk_w, uint16_t* out, uint32_t* status, int num_sms, cudaStream_t st);
 
 // Diagnostic: one thread waits on an mbarrier that nothing arrives on, through
 // the library's bounded wait; records kStatusTimeout after kWaitLimitNs.
