@@ -414,7 +414,7 @@ moe_status moe_forward(const moe_shape* shape, const float* logits, const moe_bf
   // routing, then the permutation and the row gather in one kernel
   if (launch_route_gather(sh, logits, X, v.topk_ids, v.topk_w, v.counts, v.off_pad, v.block_expert, v.num_blocks,
                           v.gather_idx, v.scatter_idx, w.local_rank, w.chunk_counts, w.xp,
-                          ws_route_counter(w.status), w.win_done, forward_counters_of(sh), w.status,
+                          ws_route_counter(w.status), w.win_done, forward_counters_of(sh), w.status, sms,
                           s) != cudaSuccess)
     return MOE_ERR_CUDA;
   // the down GEMM starts on each token window as soon as its h rows are in

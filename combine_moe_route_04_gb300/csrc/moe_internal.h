@@ -119,7 +119,8 @@ cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const u
                                 float* topk_w, int32_t* counts, int32_t* off_pad, int32_t* block_expert,
                                 int32_t* num_blocks, int32_t* gather_idx, int32_t* scatter_idx,
                                 int32_t* local_rank, int32_t* chunk_counts, uint16_t* Xp, uint32_t* route_counter,
-                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, cudaStream_t st);
+                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, int num_sms,
+                                cudaStream_t st);
 
 // Xp[scatter_idx[t, j]] = X[t] for every (t, j), token by token (each row of
 // X read once).

@@ -388,7 +388,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int E, int k,
 }
 
 // Inside moe_forward, kernel 2 and the row gather in one: the shared part,
-// then one warp per (token, 1024 columns of X): lanes j < k find the rows of
+// then one warp per (token, piece_cols columns of X; 1024, or fewer when
+// there are few tokens): lanes j < k find the rows of
 // the token's k entries (the first piece's warp writes scatter_idx and
 // gather_idx), and the warp copies that piece of X[t] to each of them, so
 // each row of X is read once.  The in-chunk ranks come in a separate buffer
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(int T, int H, int E
                                                              int32_t* __restrict__ num_blocks,
                                                              uint32_t* __restrict__ route_counter,
                                                              uint32_t* __restrict__ fwd_counters, int64_t n_fwd,
-                                                             uint32_t* __restrict__ status) {
+                                                             int piece_cols, uint32_t* __restrict__ status) {
   __shared__ int32_t s_off[kMaxE + 1];
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ int32_t s_warp[8];
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(int T, int H, int E
   permute_common(E, nch, static_cast<int64_t>(T) * k, max_blocks, counts, s_off, s_cnt, s_warp, gather_idx, off_pad,
                  block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
   const int64_t max_rows = max_blocks * kRowBlock;
-  constexpr int CH = kGatherCols;  // columns per work item: 16 bytes x 4 per lane
+  const int CH = piece_cols;  // columns per work item: 16 bytes x (piece_cols / 256) per lane
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -506,12 +507,19 @@ cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const u
                                 float* topk_w, int32_t* counts, int32_t* off_pad, int32_t* block_expert,
                                 int32_t* num_blocks, int32_t* gather_idx, int32_t* scatter_idx,
                                 int32_t* local_rank, int32_t* chunk_counts, uint16_t* Xp, uint32_t* route_counter,
-                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, cudaStream_t st) {
+                                uint32_t* fwd_counters, int64_t n_fwd, uint32_t* status, int num_sms,
+                                cudaStream_t st) {
   const int nch = static_cast<int>(num_chunks_of(s));
   cudaError_t err = launch_route_topk(s, logits, topk_ids, topk_w, local_rank, chunk_counts, counts,
                                       route_counter, status, st);
   if (err != cudaSuccess) return err;
-  const int64_t items = static_cast<int64_t>(s.T) * gather_pieces_of(s);
+  // columns per work item: 1024, or down to 256 when there are few tokens,
+  // so that the items fill the resident warps (8 CTAs of 8 warps per SM)
+  int piece_cols = kGatherCols;
+  while (piece_cols > 256 && static_cast<int64_t>(s.T) * ((s.H + piece_cols - 1) / piece_cols) <
+                                 static_cast<int64_t>(num_sms) * 64)
+    piece_cols /= 2;
+  const int64_t items = static_cast<int64_t>(s.T) * ((s.H + piece_cols - 1) / piece_cols);
   const int64_t tail = static_cast<int64_t>(s.E) * kRowBlock / 256;  // enough threads for the padding rows
   int64_t blocks = (items + 7) / 8;  // 8 warps (items) per CTA
   if (blocks < tail) blocks = tail;
@@ -520,7 +528,7 @@ cudaError_t launch_route_gather(const moe_shape& s, const float* logits, const u
                    s.k, nch, static_cast<int64_t>(max_blocks_of(s)), static_cast<const int32_t*>(topk_ids),
                    static_cast<const int32_t*>(local_rank), counts,
                    static_cast<const int32_t*>(chunk_counts), X, Xp, scatter_idx, gather_idx, off_pad,
-                   block_expert, num_blocks, route_counter, fwd_counters, n_fwd, status);
+                   block_expert, num_blocks, route_counter, fwd_counters, n_fwd, piece_cols, status);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
