@@ -387,38 +387,57 @@ def run_ours(args, world, rank, local):
         if not torch.equal(b["out"], out):
             raise RuntimeError("buffer sets disagree after warm-up")
 
-    # The timed loop replays one moe_forward per buffer set recorded into a
-    # CUDA graph (the same five kernels and dependent-launch edges, without
-    # the per-call host work); if capture is refused it calls moe_forward
-    # directly.
+    # The timed loop replays CUDA graphs of recorded moe_forward calls (the
+    # same five kernels and dependent-launch edges, without the per-call host
+    # work).  One graph holds a run of G consecutive forwards (G = n_sets when
+    # the buffer sets rotate, else 10), as a model's layers sit back to back
+    # in one graph: forward j+1's routing is a dependent launch of forward j's
+    # combine, and the gap between two graph replays is paid once per G
+    # layers.  Steps past the last whole run replay one-forward graphs, which
+    # are also timed by themselves (graph_of_one_us).  If capture is refused
+    # the loop calls moe_forward directly.
+    G = n_sets if n_sets > 1 else 10
     launch = "cuda_graph"
-    graphs = [torch.cuda.CUDAGraph() for _ in sets]
+    singles = [torch.cuda.CUDAGraph() for _ in sets]
+    chain = torch.cuda.CUDAGraph()
     try:
         with torch.cuda.stream(stream):
-            for g, b in zip(graphs, sets):
+            for g, b in zip(singles, sets):
                 with torch.cuda.graph(g, stream=stream):
                     forward(b)
+            with torch.cuda.graph(chain, stream=stream):
+                for j in range(G):
+                    forward(sets[j % n_sets])
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
-            for g in graphs:
+            for g in singles:
                 g.replay()
+            chain.replay()
         torch.cuda.synchronize(dev)
         if not all_status_clean():
             raise RuntimeError("device status after a graph replay")
+        for b in sets[1:]:
+            if not torch.equal(b["out"], out):
+                raise RuntimeError("buffer sets disagree after the graph replays")
     except Exception as exc:  # noqa: BLE001 -- any capture failure falls back to direct calls
         launch = "direct calls (graph capture failed: %s)" % str(exc).splitlines()[0][:120]
-        graphs = None
+        singles = chain = None
         torch.cuda.synchronize(dev)
 
-    def step(i):
-        if graphs is not None:
-            graphs[i % n_sets].replay()
-        else:
-            forward(sets[i % n_sets])
+    def run_steps(n, chained=True):
+        # n consecutive layers, layer i on buffer set i mod n_sets
+        if singles is None:
+            for i in range(n):
+                forward(sets[i % n_sets])
+            return
+        q = n // G if chained else 0
+        for _ in range(q):
+            chain.replay()
+        for i in range(q * G, n):
+            singles[i % n_sets].replay()
 
-    # ---------------- timed region: K layers, one replay of a recorded
-    # moe_forward each (the five kernels chained with programmatic dependent
-    # launch), events on the launching stream around all K
+    # ---------------- timed region: K layers as graph replays (above), events
+    # on the launching stream around all K
     K = args.steps
     clocks = ClockSampler(local)
     if rank == 0:
@@ -430,8 +449,7 @@ def run_ours(args, world, rank, local):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for i in range(K):
-            step(i)
+        run_steps(K)
         t_end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -440,6 +458,18 @@ def run_ours(args, world, rank, local):
     total_ms = t_start.elapsed_time(t_end)
     if not all_status_clean():
         raise RuntimeError("device status after timed region")
+
+    # ---------------- the same K layers, one graph replay per layer
+    o0 = torch.cuda.Event(enable_timing=True)
+    o1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        o0.record(stream)
+        run_steps(K, chained=False)
+        o1.record(stream)
+    torch.cuda.synchronize(dev)
+    one_ms = o0.elapsed_time(o1) / K
+    if not all_status_clean():
+        raise RuntimeError("device status after the one-forward graphs")
 
     # ---------------- breakdown: the same K layers as the four C-ABI steps
     # with an event between each (the events also cut the launch overlap
@@ -592,9 +622,12 @@ def run_ours(args, world, rank, local):
                    "T": T, "H": H, "I": I, "E": E, "k": k,
                    "l2": l2_note,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": launch},
+                   "launch": launch if singles is None else
+                   "cuda_graph: %d forwards per graph, %d replays + %d one-forward replays"
+                   % (G, K // G, K % G)},
         "per_kernel_us": {n: statistics.mean(vv) * 1e3 for n, vv in parts.items()},
         "step_by_step_us": steps_ms * 1e3,
+        "graph_of_one_us": one_ms * 1e3,
         "roofline": dict(roof, kernel="grouped_gemm_window_kernel<up> (token-window CTA-pair tcgen05 grouped "
                                       "GEMM, timed through moe_grouped_gemm_up_rows)",
                          bytes_model="touched experts' W_gate and W_up once + X once (T*H*2) + h once",
