@@ -150,6 +150,40 @@ def test_forward_full_workload_sampled(oracle_mod, n):
     assert bool(torch.isfinite(out.float()).all())
 
 
+@pytest.mark.slow
+def test_forward_maximum_token_count(oracle_mod):
+    """moe_forward at the largest T the shape check accepts (2^22 tokens, with
+    the smallest H and I): 8.4 M permuted rows, 32 776 token windows, and the
+    gather and combine striding over 4 M tokens.  Routing bit-exact over every
+    token; sampled tokens' h, Y and out rows against the oracle."""
+    import combine_moe_route_04_gb300 as moe
+    T, H, I, E, k = 1 << 22, 128, 128, 8, 2
+    seed = 85
+    inp = {"logits": moe_inputs.make_logits(T, E, seed), "x": moe_inputs.make_tokens(T, H, seed)}
+    inp["w_gate"], inp["w_up"], inp["w_down"] = moe_inputs.make_weights(E, H, I, seed)
+    s, ws, dev, out = _forward(moe, (T, H, I, E, k), inp)
+    ref_route = oracle_mod.route(inp["logits"], k)
+    v = _view_arrays(moe, s, ws)
+    assert v["num_blocks"] == ref_route.num_blocks
+    assert np.array_equal(v["topk_ids"], ref_route.topk_ids)
+    assert np.array_equal(v["counts"], ref_route.counts)
+    assert np.array_equal(v["off_pad"], ref_route.off_pad)
+    assert np.array_equal(v["gather_idx"], ref_route.gather_idx)
+    assert np.array_equal(v["scatter_idx"], ref_route.scatter_idx)
+    assert ulp_dist_f32(v["topk_w"], ref_route.topk_w).max() <= W_ULPS
+    rng = np.random.default_rng(185)
+    toks = _sample_tokens(ref_route, T, rng)
+    o_ref, h_ref, y_ref = oracle_mod.tokens_out(toks, ref_route.topk_ids, ref_route.topk_w,
+                                                inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                                                want_rows=True)
+    rows = ref_route.scatter_idx[toks].ravel()
+    assert_rows_close(_rows_of(ws, v["h_ptr"], rows, I), h_ref.reshape(-1, I), "h rows")
+    assert_rows_close(_rows_of(ws, v["Y_ptr"], rows, H), y_ref.reshape(-1, H), "Y rows")
+    assert_rows_close(host_u16(out)[toks], o_ref, "out (sampled tokens)")
+    import torch
+    assert bool(torch.isfinite(out.float()).all())
+
+
 def _whole_rows(ws, ptr, nrows, width):
     import torch
     off = ptr - ws.data_ptr()

@@ -51,7 +51,9 @@ def test_route_workloads(oracle_mod, n):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 1, 1), (1, 8, 8), (33, 256, 16), (4097, 64, 8), (31, 5, 5),
-                                   (2, 256, 1)])
+                                   (2, 256, 1),
+                                   (1 << 18, 256, 16),   # E and k at their limits: 4.2 M rows, 8192 chunks
+                                   (1 << 22, 8, 2)])     # T at its limit: 131 072 chunks per expert scan
 def test_route_edge_shapes(oracle_mod, T, E, k):
     rng = np.random.default_rng(T + 17 * E + k)
     logits = rng.standard_normal((T, E)).astype(np.float32)
