@@ -201,6 +201,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Number of SM identifiers on the device (%nsmid: the largest SM id + 1).
+__device__ __forceinline__ uint32_t num_sm_ids() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%nsmid;" : "=r"(n));
+  return n;
+}
+
 // L2 eviction-priority policies for cache hints (createpolicy).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

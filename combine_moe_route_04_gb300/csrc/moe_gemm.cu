@@ -369,6 +369,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       const uint64_t pol_wf = policy_evict_first();
       uint32_t it = 0;
       bool stop = false;
+      // down GEMM in a forward whose gate/up GEMM is one wave of tiles (at
+      // most one per CTA pair the GPU holds; win_target counts one arrival
+      // per epilogue warp of both CTAs for each of a window's column tiles):
+      // its CTAs wait for windows on SMs the gate/up GEMM leaves idle, so
+      // each tile's first weight slices are loaded during that wait.
+      const int64_t up_tiles = static_cast<int64_t>(s_win_off[E]) * (win_target / (2u * S_EPI_WARPS));
+      const bool early_weights = !kUp && tracked && up_tiles <= static_cast<int64_t>(num_sm_ids() / 2);
+      // first ring use retired by the abort path below (left out of the drain)
+      uint32_t retired_from = 0xFFFFFFFFu;
       // each cluster's first tile is its cluster index (no draw in front of
       // its first loads); CTA 0 draws the pair's later tiles and publishes
       // them; CTA 1 reads them
@@ -397,13 +406,6 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         };
         const WinCoord c = decode_window(tile, NT, E, s_win_off, s_offp, s_cnt, max_rows);
         if (!c.ok) record_status(status, kStatusBounds);
-        // down GEMM in a forward: this window's h rows are complete once all
-        // its gate/up tiles have counted in
-        if (!kUp && tracked && c.ok &&
-            !wait_counter_at_least(win_done + c.wid, win_target, abort_flag, status, status_before)) {
-          stop = true;
-          break;
-        }
         // a one-window expert reads this weight tile once: evict it first and
         // keep the rows, h and Y in L2; windows sharing a tile read it together
         const uint64_t pol_w = (s_win_off[c.e + 1] - s_win_off[c.e]) == 1 ? pol_wf : pol_wn;
@@ -423,18 +425,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           box_rows = 80;
         }
         const uint32_t stage_tx = 2u * static_cast<uint32_t>(2 * S_W_BYTES + box_rows * BK * 2);
-        for (int kb = 0; c.ok && kb < KB; ++kb, ++it) {
-          if (!published && kb == KB / 2 && !publish()) {
-            stop = true;
-            break;
-          }
-          const uint32_t s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) {
-            stop = true;
-            break;
-          }
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], stage_tx);
+        // stage kb of this tile: the weight tile's K slice, then the token rows
+        auto load_weights = [&](uint32_t s, int kb) {
           uint8_t* st = sStage + s * C::STAGE_BYTES;
           const uint32_t fb = full0 + 8u * s;
           const int k0 = c.e * K + kb * BK;
@@ -447,7 +439,77 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             tma_load_2d_pair(st + S_W_BYTES, &tmW0, fb, n0 + 128, k0, pol_w);
             tma_load_2d_pair(st + S_W_BYTES + B_BOX_BYTES, &tmW0, fb, n0 + 192, k0, pol_w);
           }
-          tma_load_2d_pair(st + 2 * S_W_BYTES, tmap, fb, kb * BK, trow, pol_t);
+        };
+        auto load_tokens = [&](uint32_t s, int kb) {
+          tma_load_2d_pair(sStage + s * C::STAGE_BYTES + 2 * S_W_BYTES, tmap, full0 + 8u * s, kb * BK, trow, pol_t);
+        };
+        // claims the next ring stage for this tile (its empty wait, then the
+        // expected bytes of both CTAs' loads on CTA 0's full barrier)
+        auto claim = [&](uint32_t s) {
+          if (!mbar_wait(&empty[s], ((it / C::STAGES) & 1u) ^ 1u, abort_flag, status)) return false;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], stage_tx);
+          return true;
+        };
+        // down GEMM in a forward: this window's h rows are complete once all
+        // its gate/up tiles have counted in.  The weights do not depend on
+        // them: with early_weights the first stages' weight slices (as many
+        // as the ring holds) are loaded before the wait and their token rows
+        // after it.
+        const int pre = (early_weights && c.ok) ? (KB < static_cast<int>(C::STAGES) ? KB : static_cast<int>(C::STAGES)) : 0;
+        const uint32_t it0 = it;
+        // If this CTA stops with stages claimed before the wait (weights in
+        // flight, token rows not loaded), it loads their token rows anyway
+        // (in range; the values are not used), which completes the stages'
+        // full barriers, and CTA 0 waits for those: no copy is pending when
+        // the pair exits (CTA 1 is held by the final cluster barrier until
+        // CTA 0 gets there).  The MMA issuer may or may not consume these
+        // stages, so the drain leaves them out; their earlier uses were
+        // consumed before they were claimed.
+        auto retire_claimed = [&]() {
+          const uint32_t n = it - it0;
+          for (uint32_t u = 0; u < n; ++u) load_tokens((it0 + u) % C::STAGES, static_cast<int>(u));
+          if (rank == 0) {
+            for (uint32_t u = it0; u < it; ++u) {
+              int no_abort = 0;
+              mbar_wait(&full[u % C::STAGES], (u / C::STAGES) & 1u, &no_abort, status);
+            }
+          }
+          if (n > 0) retired_from = it0;
+        };
+        for (int kb = 0; kb < pre; ++kb, ++it) {
+          if (!published && kb == KB / 2 && !publish()) {
+            stop = true;
+            break;
+          }
+          if (!claim(it % C::STAGES)) {
+            stop = true;
+            break;
+          }
+          load_weights(it % C::STAGES, kb);
+        }
+        if (stop) {
+          retire_claimed();
+          break;
+        }
+        if (!kUp && tracked && c.ok &&
+            !wait_counter_at_least(win_done + c.wid, win_target, abort_flag, status, status_before)) {
+          retire_claimed();
+          stop = true;
+          break;
+        }
+        for (int kb = 0; kb < pre; ++kb) load_tokens((it0 + kb) % C::STAGES, kb);
+        for (int kb = pre; c.ok && kb < KB; ++kb, ++it) {
+          if (!published && kb == KB / 2 && !publish()) {
+            stop = true;
+            break;
+          }
+          const uint32_t s = it % C::STAGES;
+          if (!claim(s)) {
+            stop = true;
+            break;
+          }
+          load_weights(s, kb);
+          load_tokens(s, kb);
         }
         if (stop) break;
         if (!published && !publish()) break;
@@ -465,6 +527,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       const uint32_t nst = it < C::STAGES ? it : C::STAGES;
       for (uint32_t s = 0; s < nst; ++s) {
         const uint32_t last = s + C::STAGES * ((it - 1 - s) / C::STAGES);
+        if (last >= retired_from) continue;  // retired above: copies landed, earlier uses consumed
         int no_abort = 0;
         mbar_wait(&empty[s], (last / C::STAGES) & 1u, &no_abort, status);
       }
