@@ -50,7 +50,9 @@
 //   * inside one forward the two GEMMs hand over per window: the gate/up
 //     epilogue counts each stored tile on its window's counter, and the down
 //     GEMM's producers wait for their window's count instead of for the whole
-//     gate/up grid (see the kernel's entry).
+//     gate/up grid (see the kernel's entry).  Where the gate/up GEMM is one
+//     wave of tiles, a down producer loads the weight slices of its tile's
+//     first stages while it waits and the token rows after.
 // Every wait on an mbarrier or a counter is bounded; on a timeout the kernel
 // records it in the status word, the roles stop, in-flight copies and MMAs
 // are drained (bounded) and TMEM is freed before exit.
