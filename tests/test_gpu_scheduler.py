@@ -56,6 +56,12 @@ def test_shapes_share_one_workspace(oracle_mod):
 
 
 def test_uncleared_tile_counter_is_reported_and_cleared(oracle_mod):
+    """The gate/up GEMM stops drawing at once, so most windows are never
+    stored.  On this shape the gate/up GEMM is one wave of tiles, so each
+    down producer has claimed stages and loaded their weight slices before
+    its window wait gives up: the forward must still report the bounds error
+    (no wait left to run out its time limit, which would report a timeout),
+    and the next forward must be exact."""
     torch = need_gpu()
     import combine_moe_route_04_gb300 as moe
     shape, seed = SHAPES[0][:5], SHAPES[0][5]
