@@ -91,3 +91,49 @@ def test_workspace_size_covers_intermediates(moe):
         mb, mr = moe.capacity(s)
         need = mr * H * 2 * 2 + mr * I * 2 + T * k * 12 + mr * 4
         assert moe.workspace_size(s) >= need
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "moe.h"
+
+int main(void) {
+    moe_shape s = {2048, 4096, 1536, 64, 8};
+    moe_shape bad = {2048, 4096, 1536, 64, 65};   /* k > E */
+    int64_t mb = 0, mr = 0;
+    size_t ws = 0;
+    if (moe_capacity(&s, &mb, &mr) != MOE_OK) return 10;
+    if (moe_workspace_size(&s, &ws) != MOE_OK) return 11;
+    if (moe_workspace_size(&bad, &ws) != MOE_ERR_UNSUPPORTED_SHAPE) return 12;
+    if (moe_workspace_size(&s, NULL) != MOE_ERR_INVALID_ARG) return 13;
+    if (moe_workspace_size(&s, &ws) != MOE_OK) return 14;
+    /* argument errors come back before anything touches a device */
+    if (moe_forward(&s, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL) != MOE_ERR_INVALID_ARG) return 15;
+    if (moe_forward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL) != MOE_ERR_INVALID_ARG) return 16;
+    printf("%lld %lld %zu %s\n", (long long)mb, (long long)mr, ws, moe_status_string(MOE_ERR_TIMEOUT));
+    return 0;
+}
+"""
+
+
+def test_header_and_library_serve_a_plain_c_client(moe, tmp_path):
+    """include/moe.h compiles as strict C99 and a C program links the library
+    and calls its host-side functions (no GPU needed for these)."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(moe.lib_path())
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(moe.lib_path()),
+                    "-Wl,-rpath," + libdir], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    mb, mr, ws, name = r.stdout.split()
+    s = moe.shape(2048, 4096, 1536, 64, 8)
+    assert (int(mb), int(mr)) == moe.capacity(s)
+    assert int(ws) == moe.workspace_size(s)
+    assert name == "MOE_ERR_TIMEOUT"
