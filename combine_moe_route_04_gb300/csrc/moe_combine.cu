@@ -31,8 +31,10 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
                                                       const float* __restrict__ topk_w, int T, int H, int k,
                                                       int64_t max_rows, int ppt, uint16_t* __restrict__ out,
                                                       uint32_t* __restrict__ status) {
-  pdl_launch_dependents();
   pdl_wait();
+  // the next kernel (the next forward's routing) may launch only now, so its
+  // CTAs do not wait on SMs through the down GEMM this kernel waited for
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;

@@ -147,7 +147,6 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   __shared__ uint32_t s_mask[kMaxE];  // bit w: token w of the chunk picked expert e
   __shared__ int s_last;
 
-  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
@@ -157,6 +156,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_hist_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
   __syncthreads();
   pdl_wait();  // inputs and outputs may be in use by the previous kernel until here
+  // the next kernel's CTAs may launch only now: launched earlier, they would
+  // wait on SMs the previous kernel (a forward's combine) still needs
+  pdl_launch_dependents();
   // no scan has happened in this call yet (thread 0 of CTA 0 clears the mark
   // before its own arrival, so before the scanning CTA can set it)
   if (chunk == 0 && threadIdx.x == 0) route_counter[1] = 0u;
