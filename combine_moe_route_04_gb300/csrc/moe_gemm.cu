@@ -281,9 +281,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   // waits for its windows' counts instead of for the whole grid, so its
   // clusters start on the SMs this grid frees.  This grid then lets it launch
   // only after its own wait below (the rows and routing it reads are final;
-  // the routing cleared the counts).
+  // the routing cleared the counts); the down GEMM lets the combine launch
+  // after its producers' last loads.
   const bool tracked = win_done != nullptr;
-  if (!(kUp && tracked)) pdl_launch_dependents();
+  if (!tracked) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -526,6 +527,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
           atomicExch(sched + 1, 0u);
         }
       }
+      // down GEMM of a forward: the combine may launch once every producer
+      // has issued its last loads (launched at entry, its CTAs would wait on
+      // SMs through the whole GEMM; at exit, its launch would not overlap)
+      if (!kUp && tracked) pdl_launch_dependents();
       const uint32_t nst = it < C::STAGES ? it : C::STAGES;
       for (uint32_t s = 0; s < nst; ++s) {
         const uint32_t last = s + C::STAGES * ((it - 1 - s) / C::STAGES);
