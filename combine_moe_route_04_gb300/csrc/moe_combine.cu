@@ -111,11 +111,13 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint16_t* __restr
 
 cudaError_t launch_combine(const moe_shape& s, const uint16_t* Y, const int32_t* scatter_idx, const float* topk_w,
                            uint16_t* out, uint32_t* status, int num_sms, cudaStream_t st) {
-  // pieces per token: as many as make the items fill the resident warps
-  // (2 CTAs of 8 warps per SM), at most one per iteration of the row
+  // pieces per token: enough for the items to fill the resident warps (2
+  // CTAs of 8 warps per SM), rounded up, at most one per iteration of the
+  // row (measured: 2048 tokens in 2 pieces, 512 CTAs, forward 1.3% faster
+  // than 1 piece, 256 CTAs spread unevenly over the SMs)
   const int64_t vpr = s.H / 8;
   const int64_t iters = s.k <= 8 ? (vpr + 63) / 64 : (vpr + 31) / 32;
-  int64_t ppt = static_cast<int64_t>(num_sms) * 16 / s.T;
+  int64_t ppt = (static_cast<int64_t>(num_sms) * 16 + s.T - 1) / s.T;
   if (ppt < 1) ppt = 1;
   if (ppt > iters) ppt = iters;
   int64_t blocks = (static_cast<int64_t>(s.T) * ppt + 7) / 8;  // 8 warps (items) per CTA
