@@ -109,3 +109,35 @@ def test_back_to_back_forwards_keep_counters_clean(shape, bias):
         got = _forward(moe, s, d, ws)
         assert moe.last_device_status(ws) == 0, "forward %d" % i
         assert torch.equal(got, ref), "forward %d" % i
+
+
+def test_mixed_launch_regimes_queued_on_one_stream():
+    """Forwards whose kernels let their dependents launch at different points,
+    queued back to back on one stream with no host synchronisation, each
+    layer on its own workspace.  The tiny layer's permutation lets the gate/up
+    GEMM launch at entry (small gather) and its down GEMM loads weight slices
+    before its window waits (one-wave gate/up GEMM); the decode and
+    pages-shaped layers launch the gate/up GEMM after the permutation's wait;
+    the fourth layer sits between.  Every output equals the step calls'."""
+    torch = need_gpu()
+    import combine_moe_route_04_gb300 as moe
+    shapes = [((128, 256, 512, 8, 2), "none"), ((96, 2048, 512, 32, 4), "none"),
+              ((64, 4096, 1536, 64, 8), "none"), ((2048, 4096, 1536, 64, 8), "none")]
+    cases = []
+    for i, (sh, bias) in enumerate(shapes):
+        s = moe.shape(*sh)
+        d = _inputs(sh, 74 + i, bias)
+        ws = moe.alloc_workspace(s)
+        ref = _steps(moe, s, d, ws)
+        assert moe.last_device_status(ws) == 0
+        outs = [torch.empty((s.T, s.H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        cases.append((s, d, ws, ref, outs))
+    torch.cuda.synchronize()
+    for r in range(12):
+        for s, d, ws, _, outs in cases:
+            moe.moe_forward(s, d["logits"], d["x"], d["wg"], d["wu"], d["wd"], outs[r % 2], ws)
+    torch.cuda.synchronize()
+    for s, d, ws, ref, outs in cases:
+        assert moe.last_device_status(ws) == 0
+        for o in outs:
+            assert torch.equal(o, ref)
